@@ -1,0 +1,192 @@
+/*
+ * ringattn.h: C ABI of the GB300 (sm_103a) blockwise ring-attention library.
+ *
+ * What the library computes: exact softmax attention of every local Q shard
+ * against every K/V shard of a sequence split into N shards, each block giving
+ * its output and its log-sum-exp, with the partial results merged across the
+ * ring steps by the online-softmax rule.  On one GPU the "ring" is a loop over
+ * (Q shard, KV shard) pairs in HBM.
+ *
+ * Pages that define the operations (cited by title and section):
+ *   [README]  "Ring Flash Attention" README, github.com/zhuzilin/ring-flash-attention:
+ *             the API list (ring / zigzag / stripe, varlen with one cu_seqlens),
+ *             "The main idea is to use the softmax_lse output", "Limits" (fp32
+ *             accumulation across blocks).
+ *   [GUIJIA]  guijiagi.com "Ring Attention：突破百万 Token 上下文的分布式注意力":
+ *             "详细流程" (ring order), "在线 Softmax：关键技巧" (merge rule),
+ *             "Striped Ring Attention", "Zigzag Ring Attention",
+ *             "2. 显存预分配" (caller-preallocated buffers).
+ *   [AINEWS]  ainews.cool ring-flash-attention article, "技术深度解析".
+ *   [STRIPED] briefgpt.xyz abstract of "Striped Attention" (causal imbalance).
+ *
+ * Conventions shared by every call
+ *   - Tensors are described by ra_tensor: a DEVICE pointer, a dtype, and up to
+ *     four dimensions with ELEMENT strides.  The last dimension must be
+ *     contiguous (stride 1) unless a call says otherwise.
+ *   - Sequence tensors are in LAYOUT ORDER: the N shards concatenated along the
+ *     sequence axis, i.e. what the N ranks of the ring would hold.  Use
+ *     ring_attn_permute / ring_attn_unpermute to move between original token
+ *     order and layout order.
+ *   - Ownership: the caller allocates every tensor and the workspace; the
+ *     library never allocates or frees device memory and keeps no pointer
+ *     after a call returns ([GUIJIA] "2. 显存预分配").
+ *   - Streams: every call is asynchronous on `stream` (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).
+ *   - Errors: argument errors are returned synchronously before any launch;
+ *     a failed launch returns RA_ERR_CUDA.  Device-side failures (a bounded
+ *     wait that ran out) are reported by ring_attn_check_device_error.  On
+ *     any error the outputs are unspecified.
+ *   - Layout constraints for attention calls: head_dim d in {64, 128}; q, k,
+ *     v (and out, dout, dq, dk, dv) have the same shape; every stride but the
+ *     last is a multiple of 8 elements and every base pointer is 16-byte
+ *     aligned (TMA tiles), else RA_ERR_ALIGNMENT.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Shard layouts ([README] API list; [GUIJIA] "Striped Ring Attention",
+ * "Zigzag Ring Attention"; [AINEWS] contiguous blocks).  With L = s / N:
+ *   CONTIGUOUS: shard r holds original tokens [r*L, (r+1)*L).
+ *   ZIGZAG:     2N chunks of c = s / (2N); shard r holds chunk r then chunk 2N-1-r.
+ *   STRIPE:     shard r holds tokens t with t mod N == r, in increasing order. */
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_STRIPE = 2 } ra_layout;
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1, /* bad pointer, shape, dtype, layout, scale or size */
+  RA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head_dim 96) */
+  RA_ERR_ALIGNMENT = 3,   /* stride or base pointer unusable for TMA tiles */
+  RA_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than ring_attn_workspace_size */
+  RA_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  RA_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (see check_device_error) */
+  RA_ERR_DEVICE = 7       /* other device-side error (e.g. misaligned shared memory) */
+} ra_status;
+
+typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype;
+
+typedef struct {
+  void* data;        /* device pointer */
+  int32_t dtype;     /* ra_dtype */
+  int32_t ndim;      /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4]; /* in elements */
+} ra_tensor;
+
+typedef enum { RA_OP_FWD = 0, RA_OP_BWD = 1 } ra_op;
+
+/* ring_attn_fwd: the ring forward with the LSE merge fused in fp32.
+ *   q, k, v: (b, h, s, d) bf16, layout order.  out: (b, h, s, d) bf16, layout
+ *   order.  lse: (b, h, s) fp32, natural log, layout order.
+ *   For each Q shard r the kernel visits KV shards (r - t) mod N for ring steps
+ *   t = 0..N-1 ([GUIJIA] "详细流程"), computes each block with tcgen05 MMAs,
+ *   and folds it into a running fp32 (max, sum, output) state, which is the
+ *   merge of [GUIJIA] "在线 Softmax：关键技巧" kept in fp32 across blocks
+ *   ([README] "Limits").  causal: key allowed iff its original token index
+ *   <= the query's.  softmax_scale: finite and > 0 (usually 1/sqrt(d)).
+ *   workspace: may be NULL (the forward needs none). */
+ra_status ring_attn_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v, int32_t layout,
+                        int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* out, ra_tensor* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ring_attn_fwd_step: one ring step on its own, every block emitting its own
+ * result, as one rank of the ring does per step ([README] "use the
+ * softmax_lse output").  For every Q shard r, attends to KV shard (r - step)
+ * mod N only, and writes the normalised block output out_blk (b, h, s, d),
+ * bf16 or fp32, and lse_blk (b, h, s) fp32.  A row with no allowed key gets
+ * out_blk = 0 and lse_blk = -inf.  Combine the N steps with lse_merge. */
+ra_status ring_attn_fwd_step(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v, int32_t layout,
+                             int32_t n_shards, int32_t causal, float softmax_scale, int32_t step,
+                             ra_tensor* out_blk, ra_tensor* lse_blk, void* stream);
+
+/* lse_merge: out_acc, lse_acc <- merge(out_acc, lse_acc, out_blk, lse_blk),
+ * row by row, in place ([GUIJIA] "在线 Softmax：关键技巧", with each side's
+ * (max, sum) taken as (lse, 1)):
+ *   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
+ *   out_acc += w * (out_blk - out_acc).
+ * lse_blk = -inf leaves the row unchanged; lse_acc = -inf takes the block.
+ *   out_acc: (..., rows, d) fp32; lse_acc: (..., rows) fp32; out_blk: same
+ *   shape as out_acc, bf16 or fp32; lse_blk: same shape as lse_acc.  2-D to
+ *   4-D; d contiguous, d a multiple of 4, rows 16-byte aligned. */
+ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out_blk, const ra_tensor* lse_blk,
+                    void* stream);
+
+/* ring_attn_bwd: gradients of exact attention given the forward's out and lse.
+ *   dout, q, k, v, out: (b, h, s, d) bf16 layout order; lse: (b, h, s) fp32.
+ *   dq, dk, dv: (b, h, s, d) bf16 outputs, layout order.
+ *   With P = exp(S - lse) recomputed from the saved lse:
+ *   D = rowsum(dO * O), dV = P^T dO, dS = P * (dO V^T - D), dQ = scale dS K,
+ *   dK = scale dS^T Q.  dK and dV stay tile-local in tensor memory; dQ is
+ *   accumulated in fp32 in the workspace and cast at the end.
+ *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d) bytes,
+ *   256-byte aligned, owned by the caller, contents need not be initialised. */
+ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                        const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
+                        int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Varlen (packed) forms ([README] API list, "the varlen versions only support
+ * passing one cu_seqlens").  q, k, v, out: 3-D (total, h, d) or (h, total, d)
+ * bf16, given by strides (dimension 0 of shape is the one whose size is
+ * `total` when shape[0] == total, else dimension 1 must be total); lse:
+ * (h, total) fp32.  cu_seqlens_dev / cu_seqlens_host: the same int32 array of
+ * n_seqs + 1 prefix sums (0 = cu[0] <= cu[1] <= ... <= cu[n_seqs] = total);
+ * the host copy is validated before launch, the device copy is read by the
+ * kernels.  Shards are contiguous slices of the packed buffer (total / N
+ * tokens each); attention is confined to each sequence.  Only the contiguous
+ * layout is supported. */
+ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                               const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                               int32_t max_seqlen, int32_t n_shards, int32_t causal, float softmax_scale,
+                               ra_tensor* out, ra_tensor* lse, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                               const ra_tensor* out, const ra_tensor* lse, const int32_t* cu_seqlens_dev,
+                               const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen,
+                               int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk,
+                               ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ring_attn_permute: original token order -> layout order along seq_dim:
+ *   y[..., p, ...] = x[..., g(p), ...], g(p) = original token at layout position p.
+ * ring_attn_unpermute: the inverse, x[..., g(p), ...] = y[..., p, ...].
+ *   x, y: same shape, 1-D to 4-D, bf16 or fp32 (same dtype); the dimensions
+ *   after seq_dim must be packed (row-major contiguous).  A bit copy. */
+ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, int32_t n_shards, int32_t seq_dim,
+                            void* stream);
+ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,
+                              void* stream);
+
+/* Workspace bytes needed by `op` (ra_op) for (b, h, s, d); 0 for RA_OP_FWD.
+ * RA_OP_BWD: an fp32 dQ accumulator (b*h*s*d) and D = rowsum(dO*O) (b*h*s). */
+size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d);
+
+/* Synchronises `stream`, then reads and clears this device's error word.
+ * Returns RA_OK, RA_ERR_TIMEOUT (a bounded wait ran out: the kernel gave up
+ * and returned) or RA_ERR_DEVICE; RA_ERR_CUDA if the synchronisation failed.
+ * *info (optional) gets the failing wait site and block. */
+ra_status ring_attn_check_device_error(void* stream, int32_t* info);
+
+/* Debug knobs (process-wide).  RA_KNOB_WAIT_LIMIT_NS: the bounded-wait limit
+ * in ns (default 4e9).  RA_KNOB_DEBUG_FLAGS: bit 0 makes the forward's TMA
+ * producer skip the Q tile load, so that every consumer's bounded wait runs
+ * out: a test of the timeout path that hangs nothing. */
+typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1 } ra_knob;
+ra_status ring_attn_set_knob(int32_t knob, int64_t value);
+
+const char* ra_status_string(int32_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t ring_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

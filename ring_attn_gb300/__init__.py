@@ -1,0 +1,296 @@
+"""Python binding of libringattn (GB300 / sm_103a blockwise ring attention).
+
+Every call marshals torch tensors into the C ABI declared in
+``include/ringattn.h`` and launches the library's CUDA kernels on the current
+torch stream.  torch only provides device memory and streams; no step of the
+computation runs in Python or in torch.  There is no fallback: if the shared
+library is missing or a tensor is not on a CUDA device the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "LAYOUTS", "RingAttnError", "lib_path", "load", "ring_attn_fwd", "ring_attn_fwd_step", "ring_attn_bwd",
+    "ring_attn_varlen_fwd", "ring_attn_varlen_bwd", "lse_merge", "ring_attn_permute", "ring_attn_unpermute",
+    "ring_attn_workspace_size", "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_version",
+    "EXPORTED_SYMBOLS",
+]
+
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
+RA_BF16, RA_FP32 = 0, 1
+RA_OP_FWD, RA_OP_BWD = 0, 1
+RA_KNOB_WAIT_LIMIT_NS, RA_KNOB_DEBUG_FLAGS = 0, 1
+
+# Every extern "C" symbol include/ringattn.h declares.
+EXPORTED_SYMBOLS = (
+    "ring_attn_fwd", "ring_attn_fwd_step", "lse_merge", "ring_attn_bwd", "ring_attn_varlen_fwd",
+    "ring_attn_varlen_bwd", "ring_attn_permute", "ring_attn_unpermute", "ring_attn_workspace_size",
+    "ring_attn_check_device_error", "ring_attn_set_knob", "ra_status_string", "ring_attn_version",
+)
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libringattn.so")
+
+
+def load():
+    """Loads libringattn.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with ring_attn_gb300.build.build() "
+                           "(or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    T = ctypes.POINTER(_Tensor)
+    sig = {
+        "ring_attn_fwd": [T, T, T, I32, I32, I32, F32, T, T, P, SZ, P],
+        "ring_attn_fwd_step": [T, T, T, I32, I32, I32, F32, I32, T, T, P],
+        "lse_merge": [T, T, T, T, P],
+        "ring_attn_bwd": [T, T, T, T, T, T, I32, I32, I32, F32, T, T, T, P, SZ, P],
+        "ring_attn_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, F32, T, T, P, SZ, P],
+        "ring_attn_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
+        "ring_attn_permute": [T, T, I32, I32, I32, P],
+        "ring_attn_unpermute": [T, T, I32, I32, I32, P],
+        "ring_attn_check_device_error": [P, ctypes.POINTER(I32)],
+        "ring_attn_set_knob": [I32, I64],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = I32
+    lib.ring_attn_workspace_size.argtypes = [I32, I64, I64, I64, I64]
+    lib.ring_attn_workspace_size.restype = SZ
+    lib.ra_status_string.argtypes = [I32]
+    lib.ra_status_string.restype = ctypes.c_char_p
+    lib.ring_attn_version.argtypes = []
+    lib.ring_attn_version.restype = I32
+    _LIB = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load().ra_status_string(status).decode()
+        raise RingAttnError(status, f"{what}: {msg}")
+
+
+def _layout(layout) -> int:
+    if isinstance(layout, str):
+        if layout not in LAYOUTS:
+            raise ValueError(f"unknown layout {layout!r}")
+        return LAYOUTS[layout]
+    return int(layout)
+
+
+def _t(x: torch.Tensor) -> _Tensor:
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError("ring_attn_gb300 takes CUDA tensors only")
+    if x.dtype == torch.bfloat16:
+        dt = RA_BF16
+    elif x.dtype == torch.float32:
+        dt = RA_FP32
+    else:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    if x.dim() > 4 or x.dim() < 1:
+        raise ValueError("tensors must have 1 to 4 dimensions")
+    t = _Tensor()
+    t.data = x.data_ptr()
+    t.dtype = dt
+    t.ndim = x.dim()
+    for i in range(x.dim()):
+        t.shape[i] = x.shape[i]
+        t.stride[i] = x.stride(i)
+    return t
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _scale(scale, d):
+    return float(1.0 / math.sqrt(d) if scale is None else scale)
+
+
+def ring_attn_fwd(q, k, v, layout="contiguous", n_shards=1, causal=False, softmax_scale=None, out=None, lse=None,
+                  stream=None):
+    """Ring forward with the fp32 LSE merge fused.  q, k, v: (b, h, s, d) bf16 in layout order.
+
+    Returns (out (b, h, s, d) bf16, lse (b, h, s) fp32), both in layout order."""
+    lib = load()
+    b, h, s, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, h, s), dtype=torch.float32, device=q.device)
+    tq, tk, tv, to, tl = _t(q), _t(k), _t(v), _t(out), _t(lse)
+    _check(lib.ring_attn_fwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), _layout(layout), int(n_shards),
+                             int(bool(causal)), _scale(softmax_scale, d), ctypes.byref(to), ctypes.byref(tl),
+                             None, 0, _stream(stream)), "ring_attn_fwd")
+    return out, lse
+
+
+def ring_attn_fwd_step(q, k, v, step, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
+                       out_blk=None, lse_blk=None, out_dtype=torch.float32, stream=None):
+    """One ring step: every Q shard r against KV shard (r - step) mod N; block out and lse."""
+    lib = load()
+    b, h, s, d = q.shape
+    if out_blk is None:
+        out_blk = torch.empty((b, h, s, d), dtype=out_dtype, device=q.device)
+    if lse_blk is None:
+        lse_blk = torch.empty((b, h, s), dtype=torch.float32, device=q.device)
+    tq, tk, tv, to, tl = _t(q), _t(k), _t(v), _t(out_blk), _t(lse_blk)
+    _check(lib.ring_attn_fwd_step(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), _layout(layout),
+                                  int(n_shards), int(bool(causal)), _scale(softmax_scale, d), int(step),
+                                  ctypes.byref(to), ctypes.byref(tl), _stream(stream)), "ring_attn_fwd_step")
+    return out_blk, lse_blk
+
+
+def lse_merge(out_acc, lse_acc, out_blk, lse_blk, stream=None):
+    """In-place merge of a block result into (out_acc fp32, lse_acc fp32)."""
+    lib = load()
+    a, b_, c, d = _t(out_acc), _t(lse_acc), _t(out_blk), _t(lse_blk)
+    _check(lib.lse_merge(ctypes.byref(a), ctypes.byref(b_), ctypes.byref(c), ctypes.byref(d), _stream(stream)),
+           "lse_merge")
+    return out_acc, lse_acc
+
+
+def ring_attn_workspace_size(op, b, h, s, d) -> int:
+    return int(load().ring_attn_workspace_size(int(op), int(b), int(h), int(s), int(d)))
+
+
+def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv), bf16, layout order."""
+    lib = load()
+    b, h, s, d = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, b, h, s, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    r = [ctypes.byref(x) for x in ts]
+    _check(lib.ring_attn_bwd(r[0], r[1], r[2], r[3], r[4], r[5], _layout(layout), int(n_shards), int(bool(causal)),
+                             _scale(softmax_scale, d), r[6], r[7], r[8], ctypes.c_void_p(workspace.data_ptr()),
+                             workspace.numel() * workspace.element_size(), _stream(stream)), "ring_attn_bwd")
+    return dq, dk, dv
+
+
+def _cu_pair(cu_seqlens, device):
+    if isinstance(cu_seqlens, torch.Tensor):
+        host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    else:
+        host = torch.tensor(list(cu_seqlens), dtype=torch.int32)
+    dev = host.to(device)
+    return host, dev
+
+
+def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
+                         out=None, lse=None, stream=None):
+    """Packed sequences, one cu_seqlens.  q, k, v: (total, h, d) or (h, total, d) bf16.
+
+    Returns (out like q, lse (h, total) fp32)."""
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, q.device)
+    n = host.numel() - 1
+    total = int(host[-1])
+    if max_seqlen is None:
+        max_seqlen = int((host[1:] - host[:-1]).max())
+    h = q.shape[1] if q.shape[0] == total else q.shape[0]
+    d = q.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((h, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    tq, tk, tv, to, tl = _t(q), _t(k), _t(v), _t(out), _t(lse)
+    _check(lib.ring_attn_varlen_fwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                    ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()), n,
+                                    int(max_seqlen), int(n_shards), int(bool(causal)), _scale(softmax_scale, d),
+                                    ctypes.byref(to), ctypes.byref(tl), None, 0, _stream(stream)),
+           "ring_attn_varlen_fwd")
+    return out, lse
+
+
+def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
+                         softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, q.device)
+    n = host.numel() - 1
+    total = int(host[-1])
+    if max_seqlen is None:
+        max_seqlen = int((host[1:] - host[:-1]).max())
+    h = q.shape[1] if q.shape[0] == total else q.shape[0]
+    d = q.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, 1, h, total, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    r = [ctypes.byref(x) for x in ts]
+    _check(lib.ring_attn_varlen_bwd(r[0], r[1], r[2], r[3], r[4], r[5], ctypes.c_void_p(dev.data_ptr()),
+                                    ctypes.c_void_p(host.data_ptr()), n, int(max_seqlen), int(n_shards),
+                                    int(bool(causal)), _scale(softmax_scale, d), r[6], r[7], r[8],
+                                    ctypes.c_void_p(workspace.data_ptr()),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ring_attn_varlen_bwd")
+    return dq, dk, dv
+
+
+def ring_attn_permute(x, layout, n_shards, seq_dim=2, out=None, stream=None):
+    """Original token order -> layout order along seq_dim (bit copy)."""
+    lib = load()
+    out = torch.empty_like(x) if out is None else out
+    a, b_ = _t(x), _t(out)
+    _check(lib.ring_attn_permute(ctypes.byref(a), ctypes.byref(b_), _layout(layout), int(n_shards), int(seq_dim),
+                                 _stream(stream)), "ring_attn_permute")
+    return out
+
+
+def ring_attn_unpermute(y, layout, n_shards, seq_dim=2, out=None, stream=None):
+    """Layout order -> original token order along seq_dim (bit copy)."""
+    lib = load()
+    out = torch.empty_like(y) if out is None else out
+    a, b_ = _t(y), _t(out)
+    _check(lib.ring_attn_unpermute(ctypes.byref(a), ctypes.byref(b_), _layout(layout), int(n_shards),
+                                   int(seq_dim), _stream(stream)), "ring_attn_unpermute")
+    return out
+
+
+def ring_attn_check_device_error(stream=None):
+    """Synchronises the stream and returns (status, info); status 0 = no device-side error."""
+    info = ctypes.c_int32(0)
+    st = load().ring_attn_check_device_error(_stream(stream), ctypes.byref(info))
+    return int(st), int(info.value)
+
+
+def ring_attn_set_knob(knob: int, value: int):
+    _check(load().ring_attn_set_knob(int(knob), int(value)), "ring_attn_set_knob")
+
+
+def ring_attn_version() -> int:
+    return int(load().ring_attn_version())

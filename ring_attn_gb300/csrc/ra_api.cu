@@ -1,0 +1,559 @@
+// C-ABI entry points: argument validation, TMA tensor maps, workspace layout
+// and kernel launches.  Every argument error is returned before any launch.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/ringattn.h"
+#include "ra_internal.h"
+
+namespace {
+
+using namespace ra;
+
+__device__ int g_dev_err[2];  // [0] error code, [1] site | block << 8
+
+std::mutex g_mu;
+unsigned long long g_wait_limit_ns = 4000000000ull;
+int g_debug_flags = 0;
+int* g_err_ptr[64] = {nullptr};
+
+ra_status dev_ctl(DevCtl* c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess || !p) return RA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  c->err_word = g_err_ptr[dev];
+  c->err_info = g_err_ptr[dev] + 1;
+  c->wait_limit_ns = g_wait_limit_ns;
+  c->debug_flags = g_debug_flags;
+  return RA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// (b, h, s, d) view of a bf16 tensor with element strides.
+struct Bhsd {
+  void* data;
+  long long b, h, s, d;
+  long long sb, sh, ss;
+};
+
+// TMA map over (d, s, h, b) with 128 x 64 boxes and 128-byte swizzle.
+ra_status make_tmap(const Bhsd& t, CUtensorMap* m) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return RA_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)t.d, (cuuint64_t)t.s, (cuuint64_t)t.h, (cuuint64_t)t.b};
+  long long sb = t.b > 1 ? t.sb : t.sh * t.h;  // any legal stride for a size-1 dimension
+  if (sb <= 0) sb = 8;
+  long long sh = t.h > 1 ? t.sh : (t.ss * t.s > 0 ? t.ss * t.s : 8);
+  cuuint64_t strides[3] = {(cuuint64_t)(t.ss * 2), (cuuint64_t)(sh * 2), (cuuint64_t)(sb * 2)};
+  cuuint32_t box[4] = {64, (cuuint32_t)kTileM, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.data, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RA_OK : RA_ERR_ALIGNMENT;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks a bf16 (b, h, s, d) tensor usable by the tiled kernels.
+ra_status check_bhsd(const ra_tensor* t, Bhsd* v) {
+  if (!t || !t->data) return RA_ERR_INVALID_ARG;
+  if (t->ndim != 4 || t->dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (t->shape[i] < 1) return RA_ERR_INVALID_ARG;
+  if (t->stride[3] != 1) return RA_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (t->stride[i] <= 0 || t->stride[i] % 8 != 0) return RA_ERR_ALIGNMENT;
+  if (!aligned(t->data, 16)) return RA_ERR_ALIGNMENT;
+  *v = Bhsd{t->data, t->shape[0], t->shape[1], t->shape[2], t->shape[3], t->stride[0], t->stride[1], t->stride[2]};
+  return RA_OK;
+}
+
+// Varlen tensors: (total, h, d) or (h, total, d), bf16, as a b = 1 view.
+ra_status check_thd(const ra_tensor* t, long long total, Bhsd* v) {
+  if (!t || !t->data) return RA_ERR_INVALID_ARG;
+  if (t->ndim != 3 || t->dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  if (t->stride[2] != 1) return RA_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (t->shape[i] < 1) return RA_ERR_INVALID_ARG;
+  long long h, ss, sh;
+  if (t->shape[0] == total) {
+    h = t->shape[1];
+    ss = t->stride[0];
+    sh = t->stride[1];
+  } else if (t->shape[1] == total) {
+    h = t->shape[0];
+    ss = t->stride[1];
+    sh = t->stride[0];
+  } else {
+    return RA_ERR_INVALID_ARG;
+  }
+  if (ss <= 0 || sh <= 0 || ss % 8 || sh % 8) return RA_ERR_ALIGNMENT;
+  if (!aligned(t->data, 16)) return RA_ERR_ALIGNMENT;
+  *v = Bhsd{t->data, 1, h, total, t->shape[2], 0, sh, ss};
+  return RA_OK;
+}
+
+bool same_shape(const Bhsd& a, const Bhsd& b) { return a.b == b.b && a.h == b.h && a.s == b.s && a.d == b.d; }
+
+ra_status check_layout(int32_t layout, int32_t n_shards, long long s) {
+  if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_STRIPE) return RA_ERR_INVALID_ARG;
+  if (n_shards < 1 || s % n_shards != 0) return RA_ERR_INVALID_ARG;
+  if (layout == RA_LAYOUT_ZIGZAG && s % (2LL * n_shards) != 0) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+ra_status check_scale(float sc) { return (isfinite(sc) && sc > 0.f) ? RA_OK : RA_ERR_INVALID_ARG; }
+
+ra_status check_lse(const ra_tensor* t, long long b, long long h, long long s, long long* sb, long long* sh,
+                    long long* ss) {
+  if (!t || !t->data || t->dtype != RA_FP32 || !aligned(t->data, 4)) return RA_ERR_INVALID_ARG;
+  if (t->ndim == 3) {
+    if (t->shape[0] != b || t->shape[1] != h || t->shape[2] != s) return RA_ERR_INVALID_ARG;
+    *sb = t->stride[0];
+    *sh = t->stride[1];
+    *ss = t->stride[2];
+    return RA_OK;
+  }
+  if (t->ndim == 2 && b == 1) {  // varlen: (h, total)
+    if (t->shape[0] != h || t->shape[1] != s) return RA_ERR_INVALID_ARG;
+    *sb = 0;
+    *sh = t->stride[0];
+    *ss = t->stride[1];
+    return RA_OK;
+  }
+  return RA_ERR_INVALID_ARG;
+}
+
+ra_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+
+#define RA_TRY(x)                    \
+  do {                               \
+    ra_status _s = (x);              \
+    if (_s != RA_OK) return _s;      \
+  } while (0)
+
+// Shared forward: fused ring (step < 0) or one ring step.
+ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout, int32_t n_shards, int32_t causal,
+                     float scale, int32_t step, const Bhsd& o, int out_f32, float* lse, long long lsb, long long lsh,
+                     long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
+  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, o)) return RA_ERR_INVALID_ARG;
+  if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
+  RA_TRY(check_layout(layout, n_shards, q.s));
+  RA_TRY(check_scale(scale));
+  if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
+  if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  if (o.ss % (out_f32 ? 4 : 8) || o.sh % (out_f32 ? 4 : 8) || (o.b > 1 && o.sb % (out_f32 ? 4 : 8)))
+    return RA_ERR_ALIGNMENT;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = (int)q.b;
+  p.H = (int)q.h;
+  p.N = n_shards;
+  p.S = (int)q.s;
+  p.L = (int)(q.s / n_shards);
+  p.layout = layout;
+  p.causal = causal;
+  p.step = step;
+  p.n_qtiles = (p.L + kTileM - 1) / kTileM;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = o.data;
+  p.o_sb = o.sb;
+  p.o_sh = o.sh;
+  p.o_ss = o.ss;
+  p.out_f32 = out_f32;
+  p.lse = lse;
+  p.l_sb = lsb;
+  p.l_sh = lsh;
+  p.l_ss = lss;
+  p.cu = cu_dev;
+  p.n_seqs = n_seqs;
+  RA_TRY(dev_ctl(&p.ctl));
+  CUtensorMap tq, tk, tv;
+  RA_TRY(make_tmap(q, &tq));
+  RA_TRY(make_tmap(k, &tk));
+  RA_TRY(make_tmap(v, &tv));
+  return cuda_status(launch_fwd((int)q.d, tq, tk, tv, p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t bwd_ws_bytes(long long b, long long h, long long s, long long d) {
+  const size_t acc = (size_t)b * h * s * d * sizeof(float);
+  const size_t acc_al = (acc + 255) & ~(size_t)255;
+  return acc_al + (size_t)b * h * s * sizeof(float);
+}
+
+ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
+                     const float* lse, long long lsb, long long lsh, long long lss, int32_t layout, int32_t n_shards,
+                     int32_t causal, float scale, const Bhsd& dq, const Bhsd& dk, const Bhsd& dv, void* ws,
+                     size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
+  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, out) || !same_shape(q, dout) ||
+      !same_shape(q, dq) || !same_shape(q, dk) || !same_shape(q, dv))
+    return RA_ERR_INVALID_ARG;
+  if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
+  RA_TRY(check_layout(layout, n_shards, q.s));
+  RA_TRY(check_scale(scale));
+  if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
+  if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, q.d)) return RA_ERR_WORKSPACE;
+  float* dq_acc = static_cast<float*>(ws);
+  const size_t acc = (size_t)q.b * q.h * q.s * q.d * sizeof(float);
+  float* Dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + ((acc + 255) & ~(size_t)255));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  View4 vdo{dout.data, dout.sb, dout.sh, dout.ss, (int)dout.b, (int)dout.h, (int)dout.s, (int)dout.d};
+  View4 vo{out.data, out.sb, out.sh, out.ss, (int)out.b, (int)out.h, (int)out.s, (int)out.d};
+  View4 vdq{dq.data, dq.sb, dq.sh, dq.ss, (int)dq.b, (int)dq.h, (int)dq.s, (int)dq.d};
+
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = (int)q.b;
+  p.H = (int)q.h;
+  p.N = n_shards;
+  p.S = (int)q.s;
+  p.L = (int)(q.s / n_shards);
+  p.layout = layout;
+  p.causal = causal;
+  p.n_qtiles = (p.L + kTileM - 1) / kTileM;
+  p.n_ktiles = (p.L + kTileN - 1) / kTileN;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.l_sb = lsb;
+  p.l_sh = lsh;
+  p.l_ss = lss;
+  p.Dsum = Dsum;
+  p.dq_acc = dq_acc;
+  p.dk = dk.data;
+  p.dv = dv.data;
+  p.k_sb = dk.sb;
+  p.k_sh = dk.sh;
+  p.k_ss = dk.ss;
+  p.v_sb = dv.sb;
+  p.v_sh = dv.sh;
+  p.v_ss = dv.ss;
+  p.cu = cu_dev;
+  p.n_seqs = n_seqs;
+  RA_TRY(dev_ctl(&p.ctl));
+  CUtensorMap tq, tk, tv, tdo;
+  RA_TRY(make_tmap(q, &tq));
+  RA_TRY(make_tmap(k, &tk));
+  RA_TRY(make_tmap(v, &tv));
+  RA_TRY(make_tmap(dout, &tdo));
+  RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, Dsum, dq_acc, st)));
+  RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, st)));
+  return cuda_status(launch_bwd_post(dq_acc, vdq, st));
+}
+
+ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs, int32_t max_seqlen,
+                   long long* total) {
+  if (!cu_dev || !cu_host || n_seqs < 1) return RA_ERR_INVALID_ARG;
+  if (!aligned(cu_dev, 4)) return RA_ERR_ALIGNMENT;
+  if (cu_host[0] != 0) return RA_ERR_INVALID_ARG;
+  int32_t mx = 0;
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    if (cu_host[i + 1] < cu_host[i]) return RA_ERR_INVALID_ARG;
+    const int32_t len = cu_host[i + 1] - cu_host[i];
+    if (len > mx) mx = len;
+  }
+  if (max_seqlen < mx) return RA_ERR_INVALID_ARG;
+  *total = cu_host[n_seqs];
+  if (*total < 1) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ring_attn_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v, int32_t layout,
+                        int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* out, ra_tensor* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  Bhsd vq, vk, vv, vo;
+  RA_TRY(check_bhsd(q, &vq));
+  RA_TRY(check_bhsd(k, &vk));
+  RA_TRY(check_bhsd(v, &vv));
+  RA_TRY(check_bhsd(out, &vo));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
+  return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, -1, vo, 0, static_cast<float*>(lse->data),
+                    lsb, lsh, lss, nullptr, 0, stream);
+}
+
+ra_status ring_attn_fwd_step(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v, int32_t layout,
+                             int32_t n_shards, int32_t causal, float softmax_scale, int32_t step,
+                             ra_tensor* out_blk, ra_tensor* lse_blk, void* stream) {
+  Bhsd vq, vk, vv;
+  RA_TRY(check_bhsd(q, &vq));
+  RA_TRY(check_bhsd(k, &vk));
+  RA_TRY(check_bhsd(v, &vv));
+  if (n_shards < 1 || step < 0 || step >= n_shards) return RA_ERR_INVALID_ARG;
+  if (!out_blk || !out_blk->data || out_blk->ndim != 4) return RA_ERR_INVALID_ARG;
+  const int f32 = out_blk->dtype == RA_FP32;
+  if (!f32 && out_blk->dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  if (out_blk->stride[3] != 1 || !aligned(out_blk->data, 16)) return RA_ERR_ALIGNMENT;
+  Bhsd vo{out_blk->data, out_blk->shape[0], out_blk->shape[1], out_blk->shape[2], out_blk->shape[3],
+          out_blk->stride[0], out_blk->stride[1], out_blk->stride[2]};
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse_blk, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
+  return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, step, vo, f32,
+                    static_cast<float*>(lse_blk->data), lsb, lsh, lss, nullptr, 0, stream);
+}
+
+ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out_blk, const ra_tensor* lse_blk,
+                    void* stream) {
+  if (!out_acc || !lse_acc || !out_blk || !lse_blk) return RA_ERR_INVALID_ARG;
+  if (!out_acc->data || !lse_acc->data || !out_blk->data || !lse_blk->data) return RA_ERR_INVALID_ARG;
+  const int nd = out_acc->ndim;
+  if (nd < 2 || nd > 4 || out_blk->ndim != nd || lse_acc->ndim != nd - 1 || lse_blk->ndim != nd - 1)
+    return RA_ERR_INVALID_ARG;
+  if (out_acc->dtype != RA_FP32 || lse_acc->dtype != RA_FP32 || lse_blk->dtype != RA_FP32) return RA_ERR_INVALID_ARG;
+  if (out_blk->dtype != RA_FP32 && out_blk->dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  for (int i = 0; i < nd; ++i) {
+    if (out_acc->shape[i] < 1 || out_blk->shape[i] != out_acc->shape[i]) return RA_ERR_INVALID_ARG;
+    if (i < nd - 1 && (lse_acc->shape[i] != out_acc->shape[i] || lse_blk->shape[i] != out_acc->shape[i]))
+      return RA_ERR_INVALID_ARG;
+  }
+  const long long d = out_acc->shape[nd - 1];
+  if (d % 4 != 0 || 32 % (d / 4) != 0) return RA_ERR_UNSUPPORTED;
+  if (out_acc->stride[nd - 1] != 1 || out_blk->stride[nd - 1] != 1) return RA_ERR_ALIGNMENT;
+  const int bs = out_blk->dtype == RA_FP32 ? 16 : 8;  // bytes per 4 elements
+  if (!aligned(out_acc->data, 16) || !aligned(out_blk->data, bs) || !aligned(lse_acc->data, 4) ||
+      !aligned(lse_blk->data, 4))
+    return RA_ERR_ALIGNMENT;
+  MergeArgs a;
+  memset(&a, 0, sizeof(a));
+  long long n[3] = {1, 1, 1}, oa[3] = {0, 0, 0}, la[3] = {0, 0, 0}, ob[3] = {0, 0, 0}, lb[3] = {0, 0, 0};
+  const int outer = nd - 1;  // 1..3 row dimensions, right-aligned into 3 slots
+  for (int i = 0; i < outer; ++i) {
+    const int slot = 3 - outer + i;
+    n[slot] = out_acc->shape[i];
+    oa[slot] = out_acc->stride[i];
+    ob[slot] = out_blk->stride[i];
+    la[slot] = lse_acc->stride[i];
+    lb[slot] = lse_blk->stride[i];
+    if (oa[slot] % 4 || ob[slot] % 4) return RA_ERR_ALIGNMENT;
+  }
+  a.out_acc = static_cast<float*>(out_acc->data);
+  a.lse_acc = static_cast<float*>(lse_acc->data);
+  a.out_blk = out_blk->data;
+  a.lse_blk = static_cast<const float*>(lse_blk->data);
+  a.blk_f32 = out_blk->dtype == RA_FP32;
+  a.d = d;
+  a.n0 = n[0];
+  a.n1 = n[1];
+  a.n2 = n[2];
+  a.rows = n[0] * n[1] * n[2];
+  a.oa_s0 = oa[0];
+  a.oa_s1 = oa[1];
+  a.oa_s2 = oa[2];
+  a.la_s0 = la[0];
+  a.la_s1 = la[1];
+  a.la_s2 = la[2];
+  a.ob_s0 = ob[0];
+  a.ob_s1 = ob[1];
+  a.ob_s2 = ob[2];
+  a.lb_s0 = lb[0];
+  a.lb_s1 = lb[1];
+  a.lb_s2 = lb[2];
+  return cuda_status(launch_lse_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                        const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
+                        int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  Bhsd vdo, vq, vk, vv, vo, vdq, vdk, vdv;
+  RA_TRY(check_bhsd(dout, &vdo));
+  RA_TRY(check_bhsd(q, &vq));
+  RA_TRY(check_bhsd(k, &vk));
+  RA_TRY(check_bhsd(v, &vv));
+  RA_TRY(check_bhsd(out, &vo));
+  RA_TRY(check_bhsd(dq, &vdq));
+  RA_TRY(check_bhsd(dk, &vdk));
+  RA_TRY(check_bhsd(dv, &vdv));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
+  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
+                    causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                               const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                               int32_t max_seqlen, int32_t n_shards, int32_t causal, float softmax_scale,
+                               ra_tensor* out, ra_tensor* lse, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  long long total = 0;
+  RA_TRY(check_cu(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, &total));
+  Bhsd vq, vk, vv, vo;
+  RA_TRY(check_thd(q, total, &vq));
+  RA_TRY(check_thd(k, total, &vk));
+  RA_TRY(check_thd(v, total, &vv));
+  RA_TRY(check_thd(out, total, &vo));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
+  return fwd_common(vq, vk, vv, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, vo, 0,
+                    static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream);
+}
+
+ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                               const ra_tensor* out, const ra_tensor* lse, const int32_t* cu_seqlens_dev,
+                               const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen,
+                               int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk,
+                               ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  long long total = 0;
+  RA_TRY(check_cu(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, &total));
+  Bhsd vdo, vq, vk, vv, vo, vdq, vdk, vdv;
+  RA_TRY(check_thd(dout, total, &vdo));
+  RA_TRY(check_thd(q, total, &vq));
+  RA_TRY(check_thd(k, total, &vk));
+  RA_TRY(check_thd(v, total, &vv));
+  RA_TRY(check_thd(out, total, &vo));
+  RA_TRY(check_thd(dq, total, &vdq));
+  RA_TRY(check_thd(dk, total, &vdk));
+  RA_TRY(check_thd(dv, total, &vdv));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
+  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss,
+                    RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, vdq, vdk, vdv, workspace,
+                    workspace_bytes, cu_seqlens_dev, n_seqs, stream);
+}
+
+static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t layout, int32_t n_shards,
+                                int32_t seq_dim, int inverse, void* stream) {
+  if (!src || !dst || !src->data || !dst->data) return RA_ERR_INVALID_ARG;
+  const int nd = src->ndim;
+  if (nd < 1 || nd > 4 || dst->ndim != nd || src->dtype != dst->dtype) return RA_ERR_INVALID_ARG;
+  if (src->dtype != RA_BF16 && src->dtype != RA_FP32) return RA_ERR_INVALID_ARG;
+  if (seq_dim < 0 || seq_dim >= nd) return RA_ERR_INVALID_ARG;
+  for (int i = 0; i < nd; ++i)
+    if (src->shape[i] < 1 || dst->shape[i] != src->shape[i]) return RA_ERR_INVALID_ARG;
+  const long long s = src->shape[seq_dim];
+  RA_TRY(check_layout(layout, n_shards, s));
+  if (s > (1LL << 30)) return RA_ERR_UNSUPPORTED;
+  // dimensions after seq_dim must be packed in both tensors
+  long long inner = 1;
+  for (int i = nd - 1; i > seq_dim; --i) {
+    if (src->stride[i] != inner || dst->stride[i] != inner) return RA_ERR_INVALID_ARG;
+    inner *= src->shape[i];
+  }
+  const int es = src->dtype == RA_FP32 ? 4 : 2;
+  if (!aligned(src->data, es) || !aligned(dst->data, es)) return RA_ERR_ALIGNMENT;
+  PermuteArgs a;
+  memset(&a, 0, sizeof(a));
+  a.src = src->data;
+  a.dst = dst->data;
+  a.esize = es;
+  a.inner = inner;
+  for (int i = 0; i < 3; ++i) {
+    a.outer_shape[i] = 1;
+    a.src_outer_stride[i] = 0;
+    a.dst_outer_stride[i] = 0;
+  }
+  for (int i = 0; i < seq_dim; ++i) {  // right-align the outer dims into 3 slots
+    const int slot = 3 - seq_dim + i;
+    a.outer_shape[slot] = src->shape[i];
+    a.src_outer_stride[slot] = src->stride[i];
+    a.dst_outer_stride[slot] = dst->stride[i];
+  }
+  a.n_outer = a.outer_shape[0] * a.outer_shape[1] * a.outer_shape[2];
+  a.src_seq_stride = src->stride[seq_dim];
+  a.dst_seq_stride = dst->stride[seq_dim];
+  a.s = (int)s;
+  a.layout = layout;
+  a.N = n_shards;
+  a.inverse = inverse;
+  return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, int32_t n_shards, int32_t seq_dim,
+                            void* stream) {
+  return permute_common(x, y, layout, n_shards, seq_dim, 0, stream);
+}
+
+ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,
+                              void* stream) {
+  return permute_common(y, x, layout, n_shards, seq_dim, 1, stream);
+}
+
+size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d) {
+  if (b < 1 || h < 1 || s < 1 || d < 1) return 0;
+  if (op == RA_OP_BWD) return bwd_ws_bytes(b, h, s, d);
+  return 0;
+}
+
+ra_status ring_attn_check_device_error(void* stream, int32_t* info) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RA_ERR_CUDA;
+  DevCtl c;
+  RA_TRY(dev_ctl(&c));
+  int host[2] = {0, 0};
+  if (cudaMemcpy(host, c.err_word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return RA_ERR_CUDA;
+  if (host[0] != 0) {
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(c.err_word, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
+  }
+  if (info) *info = host[1];
+  if (host[0] == 0) return RA_OK;
+  return host[0] == DEV_TIMEOUT ? RA_ERR_TIMEOUT : RA_ERR_DEVICE;
+}
+
+ra_status ring_attn_set_knob(int32_t knob, int64_t value) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (knob == RA_KNOB_WAIT_LIMIT_NS) {
+    if (value < 1000) return RA_ERR_INVALID_ARG;
+    g_wait_limit_ns = (unsigned long long)value;
+    return RA_OK;
+  }
+  if (knob == RA_KNOB_DEBUG_FLAGS) {
+    if (value < 0 || value > 1) return RA_ERR_INVALID_ARG;
+    g_debug_flags = (int)value;
+    return RA_OK;
+  }
+  return RA_ERR_INVALID_ARG;
+}
+
+const char* ra_status_string(int32_t status) {
+  switch (status) {
+    case RA_OK: return "ok";
+    case RA_ERR_INVALID_ARG: return "invalid argument";
+    case RA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RA_ERR_ALIGNMENT: return "stride or pointer alignment unusable for TMA tiles";
+    case RA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case RA_ERR_CUDA: return "CUDA runtime error";
+    case RA_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case RA_ERR_DEVICE: return "device-side error";
+    default: return "unknown status";
+  }
+}
+
+int32_t ring_attn_version(void) { return 100; }
+
+}  // extern "C"

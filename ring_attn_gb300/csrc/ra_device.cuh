@@ -1,0 +1,321 @@
+// Device-side building blocks for the sm_103a kernels: mbarriers with bounded
+// waits, TMA tile loads, tcgen05 MMA / TMEM access, shared-memory operand
+// descriptors, and the shard-layout index maps.
+//
+// Every wait in this library is bounded: past a time limit (globaltimer) the
+// waiting warp records RA_ERR_TIMEOUT in the device error word, raises the
+// CTA's abort flag in shared memory and returns false, so that every role
+// leaves its loop and the CTA frees its tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ra {
+
+// ------------------------------------------------------------------ errors
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_BAD_SMEM = 7 };
+
+struct DevCtl {
+  int* err_word;          // first error code wins (atomicCAS from 0)
+  int* err_info;          // site | (block << 8) of the first failure
+  unsigned long long wait_limit_ns;
+  int debug_flags;        // bit 0: producer skips the Q load (bounded-wait test)
+};
+
+enum : int { DBG_SKIP_Q_LOAD = 1 };
+
+__device__ __forceinline__ void record_error(const DevCtl& c, int code, int site) {
+  if (atomicCAS(c.err_word, 0, code) == 0) {
+    atomicExch(c.err_info, site | (int)((blockIdx.x + blockIdx.y * gridDim.x) << 8));
+  }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One thread waits.  Returns false when the CTA aborts (own timeout or another role's).
+static __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
+                                      int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > c.wait_limit_ns) {
+        *abort_flag = 1;
+        record_error(c, DEV_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+}
+
+// A whole converged warp waits; the result is the same on every lane.
+static __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
+                                       int site) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((it & 15u) == 15u) {
+      int stop = 0;
+      if (lane_id() == 0) {
+        if (*abort_flag) {
+          stop = 1;
+        } else {
+          unsigned long long now = globaltimer();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > c.wait_limit_ns) {
+            *abort_flag = 1;
+            record_error(c, DEV_TIMEOUT, site);
+            stop = 1;
+          }
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+// Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------ TMA
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 4-D tiled load (coordinates innermost first) into shared memory; completion
+// is signalled as transaction bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Make generic-proxy writes to shared memory visible to the async proxy (MMA reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on the mbarrier when every previously issued MMA of this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Instruction descriptor for kind::f16: bf16 A and B, fp32 D, dense.
+// a_mn / b_mn: 0 = K-major, 1 = MN-major operand in shared memory.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | ((uint32_t)a_mn << 15)        // A major
+         | ((uint32_t)b_mn << 16)        // B major
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA's
+// SWIZZLE_128B writes: 8 rows of 128 B form a 1024-byte atom, and the 16-byte
+// chunk c of row r sits at chunk c ^ (r & 7)).
+//   K-major operand:  rows = M (or N) at 128 B pitch, SBO = 1024 (next 8 rows);
+//                     the start address advances 32 B per 16-element K step.
+//   MN-major operand: rows = K at 128 B pitch holding 64 consecutive MN elements;
+//                     SBO = 1024 (next 8 K rows), LBO = offset of the next 64-wide
+//                     MN block; the start advances 2048 B per 16-row K step.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` inside a 128B-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+#define RA_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                 "=r"(r[i + 6]), "=r"(r[i + 7])
+#define RA_P8(i) "+r"(r[i + 0]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]), \
+                 "+r"(r[i + 6]), "+r"(r[i + 7])
+#define RA_I8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                 "r"(r[i + 6]), "r"(r[i + 7])
+
+// Lane (32*quadrant + laneid) reads 32 consecutive 32-bit columns starting at taddr's column.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : RA_R8(0), RA_R8(8), RA_R8(16), RA_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+// Wait for outstanding tcgen05.ld; the registers are threaded through so that
+// no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : RA_P8(0), RA_P8(8), RA_P8(16), RA_P8(24) : : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      RA_I8(0), RA_I8(8), RA_I8(16), RA_I8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+#undef RA_R8
+#undef RA_P8
+#undef RA_I8
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ layouts
+// Original token index of local position i in shard r (L tokens per shard).
+enum : int { LAYOUT_CONTIGUOUS = 0, LAYOUT_ZIGZAG = 1, LAYOUT_STRIPE = 2 };
+
+__host__ __device__ __forceinline__ long long token_of(int layout, int N, int L, int r, int i) {
+  if (layout == LAYOUT_STRIPE) return (long long)i * N + r;
+  if (layout == LAYOUT_ZIGZAG) {
+    int c = L >> 1;
+    return i < c ? (long long)r * c + i : (long long)(2 * N - 1 - r) * c + (i - c);
+  }
+  return (long long)r * L + i;
+}
+
+// Largest local index j of shard s with token_of(s, j) <= g, or -1.
+__host__ __device__ __forceinline__ int last_local_at_or_before(int layout, int N, int L, int s, long long g) {
+  if (layout == LAYOUT_STRIPE) {
+    if (g < s) return -1;
+    long long j = (g - s) / N;
+    return (int)(j < L - 1 ? j : L - 1);
+  }
+  if (layout == LAYOUT_ZIGZAG) {
+    int c = L >> 1;
+    long long hi0 = (long long)(2 * N - 1 - s) * c;
+    if (g >= hi0) {
+      long long j = c + (g - hi0);
+      return (int)(j < L - 1 ? j : L - 1);
+    }
+    long long lo0 = (long long)s * c;
+    if (g >= lo0) {
+      long long j = g - lo0;
+      return (int)(j < c - 1 ? j : c - 1);
+    }
+    return -1;
+  }
+  long long j = g - (long long)s * L;
+  if (j < 0) return -1;
+  return (int)(j < L - 1 ? j : L - 1);
+}
+
+// Segment index k with cu[k] <= t < cu[k+1] (binary search, n_seqs >= 1).
+__device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs, long long t) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)__ldg(cu + mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace ra
+
+namespace ra {
+// Wait that ignores the abort flag (bounded by time only): used at teardown to
+// let copies and MMAs already in flight land before the CTA exits.
+static __device__ __noinline__ void drain_one(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
+  unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > c.wait_limit_ns) {
+      record_error(c, DEV_TIMEOUT, site);
+      return;
+    }
+  }
+}
+}  // namespace ra

@@ -1,0 +1,102 @@
+// Parameters shared between the C-ABI host code and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra_device.cuh"
+
+namespace ra {
+
+constexpr int kTileM = 128;   // query rows per tile
+constexpr int kTileN = 128;   // key rows per tile
+
+struct FwdParams {
+  int B, H, N, L, S;        // batch, heads, shards, tokens per shard, total tokens
+  int layout, causal;
+  int step;                 // -1: fused ring over all N steps; else one ring step
+  int n_qtiles;             // ceil(L / 128)
+  float scale_log2;         // softmax_scale * log2(e)
+  void* out;                // bf16 (fused) or bf16/fp32 (step mode)
+  long long o_sb, o_sh, o_ss;
+  int out_f32;
+  float* lse;
+  long long l_sb, l_sh, l_ss;
+  const int* cu;            // varlen cu_seqlens (device) or nullptr
+  int n_seqs;
+  DevCtl ctl;
+};
+
+struct BwdParams {
+  int B, H, N, L, S;
+  int layout, causal;
+  int n_qtiles, n_ktiles;   // tiles per shard
+  float scale;              // softmax scale
+  float scale_log2;
+  const float* lse;         // (b, h, s) natural log, element strides
+  long long l_sb, l_sh, l_ss;
+  const float* Dsum;        // rowsum(dO * O), packed (b, h, s)
+  float* dq_acc;            // fp32 (b, h, s, d) packed accumulator
+  void* dk;                 // bf16 outputs
+  void* dv;
+  long long k_sb, k_sh, k_ss;   // strides of dk
+  long long v_sb, v_sh, v_ss;   // strides of dv
+  const int* cu;
+  int n_seqs;
+  DevCtl ctl;
+};
+
+// Strided 4-D view of a tensor whose last dimension is contiguous.
+struct View4 {
+  void* data;
+  long long sb, sh, ss;     // element strides of dims 0..2
+  int b, h, s, d;
+};
+
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t st);
+size_t fwd_smem_bytes(int D);
+
+cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
+size_t bwd_smem_bytes(int D);
+
+// D = rowsum(dO * O) (fp32, packed (b,h,s)) and zero of the dQ accumulator.
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, float* Dsum, float* dq_acc, cudaStream_t st);
+// dq (bf16) = dq_acc (fp32, packed).
+cudaError_t launch_bwd_post(const float* dq_acc, const View4& dq, cudaStream_t st);
+
+struct MergeArgs {
+  float* out_acc;        // rows x d, row stride (elements)
+  float* lse_acc;
+  const void* out_blk;
+  const float* lse_blk;
+  int blk_f32;
+  long long rows, d;
+  // 3 outer dims (rows = o0 * o1 * o2) with their strides
+  long long n0, n1, n2;
+  long long oa_s0, oa_s1, oa_s2;
+  long long la_s0, la_s1, la_s2;
+  long long ob_s0, ob_s1, ob_s2;
+  long long lb_s0, lb_s1, lb_s2;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st);
+
+struct PermuteArgs {
+  const void* src;
+  void* dst;
+  int esize;                // bytes per element
+  long long inner;          // elements per row (packed dims after seq)
+  long long n_outer;        // product of dims before seq
+  long long outer_shape[3]; // up to 3 outer dims (unused = 1)
+  long long src_outer_stride[3], dst_outer_stride[3];
+  long long src_seq_stride, dst_seq_stride;
+  int s, layout, N;
+  int inverse;              // 0: dst[p] = src[g(p)]; 1: dst[g(p)] = src[p]
+};
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace ra

@@ -1,0 +1,223 @@
+// Memory-bound kernels of the ring-attention path: shard-layout permutation,
+// the standalone LSE merge, the backward preprocess D = rowsum(dO * O) and
+// the final cast of the fp32 dQ accumulator.  All are grid-stride loops with
+// 16-byte accesses, sized to a multiple of the SM count.
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(long long work_items, int per_block) {
+  long long blocks = (work_items + per_block - 1) / per_block;
+  long long cap = (long long)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+// ------------------------------------------------------------------ permutation
+// A "row" is the packed run of elements after the sequence dimension.  Each
+// thread moves 16 bytes when the row allows it, else one element.
+template <typename V>
+__global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, long long vec_per_row) {
+  const long long total = a.n_outer * a.s * vec_per_row;
+  const long long step = (long long)gridDim.x * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += step) {
+    const long long v = t % vec_per_row;
+    const long long rp = t / vec_per_row;
+    const int p = (int)(rp % a.s);           // layout position
+    long long o = rp / a.s;                  // outer index
+    const long long o2 = o % a.outer_shape[2];
+    o /= a.outer_shape[2];
+    const long long o1 = o % a.outer_shape[1];
+    const long long o0 = o / a.outer_shape[1];
+    const int L = a.s / a.N;
+    const long long g = token_of(a.layout, a.N, L, p / L, p % L);  // original token at position p
+    const long long src_pos = a.inverse ? p : g;
+    const long long dst_pos = a.inverse ? g : p;
+    const long long so = o0 * a.src_outer_stride[0] + o1 * a.src_outer_stride[1] + o2 * a.src_outer_stride[2] +
+                         src_pos * a.src_seq_stride;
+    const long long dof = o0 * a.dst_outer_stride[0] + o1 * a.dst_outer_stride[1] + o2 * a.dst_outer_stride[2] +
+                          dst_pos * a.dst_seq_stride;
+    const char* s = reinterpret_cast<const char*>(a.src) + so * a.esize;
+    char* d = reinterpret_cast<char*>(a.dst) + dof * a.esize;
+    reinterpret_cast<V*>(d)[v] = reinterpret_cast<const V*>(s)[v];
+  }
+}
+
+// ------------------------------------------------------------------ LSE merge
+// A group of d/4 threads (d/4 divides 32, so a group sits inside one warp)
+// owns a row, 4 columns per thread:
+//   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
+//   out_acc += w * (out_blk - out_acc).
+// Loop control is warp-uniform so that every lane of the row has read the old
+// lse_acc (before __syncwarp) before the row's first lane overwrites it.
+template <bool BLK_F32>
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
+  const long long q_per_row = a.d / 4;
+  const long long total = a.rows * q_per_row;
+  const long long step = (long long)gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x - lane; base < total; base += step) {
+    const long long t = base + lane;
+    const bool live = t < total;
+    const long long c4 = live ? t % q_per_row : 0;
+    long long rw = live ? t / q_per_row : 0;
+    const long long i2 = rw % a.n2;
+    rw /= a.n2;
+    const long long i1 = rw % a.n1;
+    const long long i0 = rw / a.n1;
+    float* oa = a.out_acc + i0 * a.oa_s0 + i1 * a.oa_s1 + i2 * a.oa_s2 + 4 * c4;
+    float* la = a.lse_acc + i0 * a.la_s0 + i1 * a.la_s1 + i2 * a.la_s2;
+    const float* lb = a.lse_blk + i0 * a.lb_s0 + i1 * a.lb_s1 + i2 * a.lb_s2;
+    const long long bofs = i0 * a.ob_s0 + i1 * a.ob_s1 + i2 * a.ob_s2 + 4 * c4;
+    const float A = live ? *la : 0.f;
+    const float B = live ? __ldg(lb) : -INFINITY;
+    __syncwarp();
+    if (!live || B == -INFINITY) continue;  // empty block: accumulator unchanged
+    float4 ob;
+    if (BLK_F32) {
+      ob = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs));
+    } else {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs));
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      ob = make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+    }
+    float4 r;
+    float lse_new;
+    if (A == -INFINITY) {
+      r = ob;  // empty accumulator: take the block
+      lse_new = B;
+    } else {
+      const float4 oacc = *reinterpret_cast<const float4*>(oa);
+      lse_new = fmaxf(A, B) + log1pf(expf(-fabsf(A - B)));
+      const float w = expf(B - lse_new);
+      r = make_float4(oacc.x + w * (ob.x - oacc.x), oacc.y + w * (ob.y - oacc.y), oacc.z + w * (ob.z - oacc.z),
+                      oacc.w + w * (ob.w - oacc.w));
+    }
+    *reinterpret_cast<float4*>(oa) = r;
+    if (c4 == 0) *la = lse_new;
+  }
+}
+
+// ------------------------------------------------------------------ backward pre / post
+// D[b,h,p] = sum_d dO * O (fp32), and the fp32 dQ accumulator row set to zero.
+// 16 threads per row of d = 128 (8 bf16 each), 8 per row of d = 64.
+__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, float* Dsum, float* dq_acc) {
+  const int tpr = dout.d / 8;  // threads per row
+  const long long rows = (long long)dout.b * dout.h * dout.s;
+  const long long total = rows * tpr;
+  const long long step = (long long)gridDim.x * blockDim.x;
+  // tpr divides 32, so each row's threads sit in one warp and stay converged
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t - threadIdx.x % 32 < total; t += step) {
+    const bool live = t < total;
+    const long long row = live ? t / tpr : 0;
+    const int part = (int)(t % tpr);
+    const long long p = row % dout.s;
+    const long long bh = row / dout.s;
+    const long long h = bh % dout.h, b = bh / dout.h;
+    float acc = 0.f;
+    if (live) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dout.data) +
+                                                           b * dout.sb + h * dout.sh + p * dout.ss) + part);
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(out.data) +
+                                                           b * out.sb + h * out.sh + p * out.ss) + part);
+      const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x);
+      const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 a = __bfloat1622float2(xv[u]);
+        const float2 c = __bfloat1622float2(yv[u]);
+        acc = fmaf(a.x, c.x, acc);
+        acc = fmaf(a.y, c.y, acc);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * dout.d) + 2 * part;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && part == 0) Dsum[row] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_post_kernel(const float* dq_acc, View4 dq) {
+  const int tpr = dq.d / 8;
+  const long long rows = (long long)dq.b * dq.h * dq.s;
+  const long long total = rows * tpr;
+  const long long step = (long long)gridDim.x * blockDim.x;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += step) {
+    const long long row = t / tpr;
+    const int part = (int)(t % tpr);
+    const long long p = row % dq.s;
+    const long long bh = row / dq.s;
+    const long long h = bh % dq.h, b = bh / dq.h;
+    const float4* src = reinterpret_cast<const float4*>(dq_acc + row * dq.d) + 2 * part;
+    const float4 u = __ldg(src), v = __ldg(src + 1);
+    uint4 o;
+    o.x = pack_bf16x2(u.x, u.y);
+    o.y = pack_bf16x2(u.z, u.w);
+    o.z = pack_bf16x2(v.x, v.y);
+    o.w = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dq.data) + b * dq.sb + h * dq.sh + p * dq.ss)[part] = o;
+  }
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
+  const long long row_bytes = a.inner * a.esize;
+  const bool vec16 = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(a.src) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(a.dst) % 16 == 0) && (a.src_seq_stride * a.esize) % 16 == 0 &&
+                     (a.dst_seq_stride * a.esize) % 16 == 0 && (a.src_outer_stride[0] * a.esize) % 16 == 0 &&
+                     (a.src_outer_stride[1] * a.esize) % 16 == 0 && (a.src_outer_stride[2] * a.esize) % 16 == 0 &&
+                     (a.dst_outer_stride[0] * a.esize) % 16 == 0 && (a.dst_outer_stride[1] * a.esize) % 16 == 0 &&
+                     (a.dst_outer_stride[2] * a.esize) % 16 == 0;
+  const long long total_rows = a.n_outer * a.s;
+  if (vec16) {
+    const long long vpr = row_bytes / 16;
+    permute_kernel<uint4><<<grid_for(total_rows * vpr, kThreads), kThreads, 0, st>>>(a, vpr);
+  } else if (a.esize == 4) {
+    permute_kernel<uint32_t><<<grid_for(total_rows * a.inner, kThreads), kThreads, 0, st>>>(a, a.inner);
+  } else {
+    permute_kernel<uint16_t><<<grid_for(total_rows * a.inner, kThreads), kThreads, 0, st>>>(a, a.inner);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
+  const long long total = a.rows * (a.d / 4);
+  if (a.blk_f32)
+    lse_merge_kernel<true><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
+  else
+    lse_merge_kernel<false><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, float* Dsum, float* dq_acc, cudaStream_t st) {
+  const long long total = (long long)dout.b * dout.h * dout.s * (dout.d / 8);
+  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, Dsum, dq_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const float* dq_acc, const View4& dq, cudaStream_t st) {
+  const long long total = (long long)dq.b * dq.h * dq.s * (dq.d / 8);
+  bwd_post_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dq_acc, dq);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

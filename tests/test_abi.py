@@ -1,0 +1,172 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ring_attn_gb300 as ra
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ring_attn_gb300.build import build
+
+    build()
+    return ra.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(ra.EXPORTED_SYMBOLS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ra_status_string(0) == b"ok"
+    assert b"workspace" in lib.ra_status_string(4)
+    assert lib.ra_status_string(99) == b"unknown status"
+    assert lib.ring_attn_version() == 100
+
+
+def test_workspace_size(lib):
+    assert lib.ring_attn_workspace_size(0, 1, 2, 256, 64) == 0
+    acc = 1 * 2 * 256 * 64 * 4
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64) == ((acc + 255) // 256) * 256 + 1 * 2 * 256 * 4
+    assert lib.ring_attn_workspace_size(1, 0, 2, 256, 64) == 0
+
+
+def _fake(shape, dtype=ra.RA_BF16, data=0x10000, strides=None):
+    t = ra._Tensor()
+    t.data = data
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if strides is None:
+        strides = []
+        acc = 1
+        for n in reversed(shape):
+            strides.insert(0, acc)
+            acc *= n
+    for i, n in enumerate(shape):
+        t.shape[i] = n
+        t.stride[i] = strides[i]
+    return t
+
+
+def _fwd(lib, q, k, v, out, lse, layout=0, n=2, causal=1, scale=0.125):
+    return lib.ring_attn_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), layout, n, causal, scale,
+                             ctypes.byref(out), ctypes.byref(lse), None, 0, None)
+
+
+def test_fwd_rejects_bad_arguments_before_launch(lib):
+    shp = (1, 2, 256, 64)
+    ok = lambda: _fake(shp)  # noqa: E731
+    lse = _fake((1, 2, 256), ra.RA_FP32)
+    # null data pointer
+    assert _fwd(lib, _fake(shp, data=0), ok(), ok(), ok(), lse) == 1
+    # wrong dtype
+    assert _fwd(lib, _fake(shp, ra.RA_FP32), ok(), ok(), ok(), lse) == 1
+    # shape mismatch
+    assert _fwd(lib, ok(), _fake((1, 2, 128, 64)), ok(), ok(), lse) == 1
+    # unsupported head dim
+    assert _fwd(lib, _fake((1, 2, 256, 96)), _fake((1, 2, 256, 96)), _fake((1, 2, 256, 96)),
+                _fake((1, 2, 256, 96)), lse) == 2
+    # s not divisible by n_shards; zigzag needs 2N
+    assert _fwd(lib, ok(), ok(), ok(), ok(), lse, n=3) == 1
+    assert _fwd(lib, _fake((1, 2, 24, 64)), _fake((1, 2, 24, 64)), _fake((1, 2, 24, 64)), _fake((1, 2, 24, 64)),
+                _fake((1, 2, 24), ra.RA_FP32), layout=1, n=8) == 1
+    # bad layout, bad causal flag, bad scale
+    assert _fwd(lib, ok(), ok(), ok(), ok(), lse, layout=3) == 1
+    assert _fwd(lib, ok(), ok(), ok(), ok(), lse, causal=2) == 1
+    assert _fwd(lib, ok(), ok(), ok(), ok(), lse, scale=0.0) == 1
+    assert _fwd(lib, ok(), ok(), ok(), ok(), lse, scale=float("nan")) == 1
+    # non-contiguous head dim and misaligned strides / pointers
+    assert _fwd(lib, _fake(shp, strides=(32768, 16384, 64, 2)), ok(), ok(), ok(), lse) == 3
+    assert _fwd(lib, _fake(shp, strides=(32768, 16384, 68, 1)), ok(), ok(), ok(), lse) == 3
+    assert _fwd(lib, _fake(shp, data=0x10008), ok(), ok(), ok(), lse) == 3
+    # lse shape
+    assert _fwd(lib, ok(), ok(), ok(), ok(), _fake((1, 2, 128), ra.RA_FP32)) == 1
+
+
+def test_bwd_rejects_missing_workspace(lib):
+    shp = (1, 2, 256, 64)
+    ts = [_fake(shp) for _ in range(5)]
+    lse = _fake((1, 2, 256), ra.RA_FP32)
+    grads = [_fake(shp) for _ in range(3)]
+    r = lib.ring_attn_bwd(*(ctypes.byref(t) for t in ts), ctypes.byref(lse), 0, 2, 1, 0.125,
+                          *(ctypes.byref(t) for t in grads), None, 0, None)
+    assert r == 4
+    r = lib.ring_attn_bwd(*(ctypes.byref(t) for t in ts), ctypes.byref(lse), 0, 2, 1, 0.125,
+                          *(ctypes.byref(t) for t in grads), ctypes.c_void_p(0x100000), 16, None)
+    assert r == 4
+
+
+def test_varlen_rejects_bad_cu_seqlens(lib):
+    q = _fake((64, 2, 64))
+    lse = _fake((2, 64), ra.RA_FP32)
+
+    def call(cu, n, maxlen=64):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        return lib.ring_attn_varlen_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), ctypes.c_void_p(0x1000),
+                                        ctypes.cast(arr, ctypes.c_void_p), n, maxlen, 2, 1, 0.125, ctypes.byref(q),
+                                        ctypes.byref(lse), None, 0, None)
+
+    assert call([1, 64], 1) == 1           # cu[0] != 0
+    assert call([0, 40, 30, 64], 3) == 1   # decreasing
+    assert call([0, 40, 64], 2, maxlen=10) == 1  # max_seqlen too small
+    assert call([0, 40, 60], 2) == 1       # total does not match the tensors
+    assert call([0, 64], 0) == 1           # no sequence
+
+
+def test_lse_merge_rejects_bad_shapes(lib):
+    oa = _fake((2, 8, 128), ra.RA_FP32)
+    la = _fake((2, 8), ra.RA_FP32)
+    ob = _fake((2, 8, 128), ra.RA_BF16)
+    lb = _fake((2, 8), ra.RA_FP32)
+    bad = _fake((2, 9, 128), ra.RA_BF16)
+    assert lib.lse_merge(ctypes.byref(oa), ctypes.byref(la), ctypes.byref(bad), ctypes.byref(lb), None) == 1
+    assert lib.lse_merge(ctypes.byref(oa), ctypes.byref(la), ctypes.byref(ob), ctypes.byref(_fake((2, 8))), None) == 1
+    big = _fake((2, 8, 256), ra.RA_FP32)
+    assert lib.lse_merge(ctypes.byref(big), ctypes.byref(la), ctypes.byref(_fake((2, 8, 256))), ctypes.byref(lb),
+                         None) == 2
+
+
+def test_permute_rejects_bad_arguments(lib):
+    x = _fake((1, 2, 12, 8))
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 10, 8))), 0, 2, 2, None) == 1
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8))), 1, 4, 2, None) == 1  # 12 % 8
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8))), 0, 2, 4, None) == 1
+    # dims after seq_dim must be packed
+    y = _fake((1, 2, 12, 8), strides=(384, 192, 16, 2))
+    assert lib.ring_attn_permute(ctypes.byref(y), ctypes.byref(_fake((1, 2, 12, 8))), 0, 2, 2, None) == 1
+
+
+def test_knobs(lib):
+    assert lib.ring_attn_set_knob(0, 10) == 1
+    assert lib.ring_attn_set_knob(1, 5) == 1
+    assert lib.ring_attn_set_knob(7, 0) == 1
+    assert lib.ring_attn_set_knob(0, 4_000_000_000) == 0
+    assert lib.ring_attn_set_knob(1, 0) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ra.ring_attn_fwd(x, x, x)
