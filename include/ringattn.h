@@ -110,7 +110,8 @@ ra_status ring_attn_fwd_step(const ra_tensor* q, const ra_tensor* k, const ra_te
  * (max, sum) taken as (lse, 1)):
  *   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
  *   out_acc += w * (out_blk - out_acc).
- * lse_blk = -inf leaves the row unchanged; lse_acc = -inf takes the block.
+ * lse_blk = -inf leaves the row unchanged; lse_acc = -inf takes the block;
+ * both -inf give out_acc = 0, lse_acc = -inf.
  *   out_acc: (..., rows, d) fp32; lse_acc: (..., rows) fp32; out_blk: same
  *   shape as out_acc, bf16 or fp32; lse_blk: same shape as lse_acc.  2-D to
  *   4-D; d contiguous, d a multiple of 4, rows 16-byte aligned. */
@@ -179,6 +180,24 @@ ra_status ring_attn_check_device_error(void* stream, int32_t* info);
  * out: a test of the timeout path that hangs nothing. */
 typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1 } ra_knob;
 ra_status ring_attn_set_knob(int32_t knob, int64_t value);
+
+/* Per-kernel timing (process-wide, off by default; one device per process).
+ * While enabled, the library brackets every kernel it launches with CUDA
+ * events recorded on the launch stream.  ring_attn_timing_read synchronises
+ * the recorded events of `kernel` (ra_kernel), returns the summed device
+ * milliseconds and the number of launches since the last read, and resets
+ * them.  Disabling drops anything not yet read. */
+typedef enum {
+  RA_KERNEL_FWD = 0,       /* ring forward (fused merge, or one ring step) */
+  RA_KERNEL_BWD = 1,       /* ring backward main kernel */
+  RA_KERNEL_BWD_PRE = 2,   /* D = rowsum(dO * O), dQ accumulator cleared */
+  RA_KERNEL_BWD_POST = 3,  /* dQ fp32 -> bf16 */
+  RA_KERNEL_PERMUTE = 4,   /* permute / unpermute */
+  RA_KERNEL_LSE_MERGE = 5,
+  RA_KERNEL_COUNT = 6
+} ra_kernel;
+ra_status ring_attn_timing_enable(int32_t on);
+ra_status ring_attn_timing_read(int32_t kernel, double* total_ms, int64_t* launches);
 
 const char* ra_status_string(int32_t status);
 

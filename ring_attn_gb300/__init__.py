@@ -18,7 +18,7 @@ __all__ = [
     "LAYOUTS", "RingAttnError", "lib_path", "load", "ring_attn_fwd", "ring_attn_fwd_step", "ring_attn_bwd",
     "ring_attn_varlen_fwd", "ring_attn_varlen_bwd", "lse_merge", "ring_attn_permute", "ring_attn_unpermute",
     "ring_attn_workspace_size", "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_version",
-    "EXPORTED_SYMBOLS",
+    "ring_attn_timing_enable", "ring_attn_timing_read", "EXPORTED_SYMBOLS", "KERNELS",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -30,8 +30,10 @@ RA_KNOB_WAIT_LIMIT_NS, RA_KNOB_DEBUG_FLAGS = 0, 1
 EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_step", "lse_merge", "ring_attn_bwd", "ring_attn_varlen_fwd",
     "ring_attn_varlen_bwd", "ring_attn_permute", "ring_attn_unpermute", "ring_attn_workspace_size",
-    "ring_attn_check_device_error", "ring_attn_set_knob", "ra_status_string", "ring_attn_version",
+    "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
+    "ra_status_string", "ring_attn_version",
 )
+KERNELS = {"fwd": 0, "bwd": 1, "bwd_pre": 2, "bwd_post": 3, "permute": 4, "lse_merge": 5}
 
 
 class RingAttnError(RuntimeError):
@@ -75,6 +77,8 @@ def load():
         "ring_attn_unpermute": [T, T, I32, I32, I32, P],
         "ring_attn_check_device_error": [P, ctypes.POINTER(I32)],
         "ring_attn_set_knob": [I32, I64],
+        "ring_attn_timing_enable": [I32],
+        "ring_attn_timing_read": [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -290,6 +294,20 @@ def ring_attn_check_device_error(stream=None):
 
 def ring_attn_set_knob(knob: int, value: int):
     _check(load().ring_attn_set_knob(int(knob), int(value)), "ring_attn_set_knob")
+
+
+def ring_attn_timing_enable(on: bool = True):
+    """Bracket every library kernel launch with CUDA events (see ring_attn_timing_read)."""
+    _check(load().ring_attn_timing_enable(int(bool(on))), "ring_attn_timing_enable")
+
+
+def ring_attn_timing_read(kernel) -> tuple:
+    """(total device ms, launches) of one kernel kind since the last read; resets it."""
+    k = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int64(0)
+    _check(load().ring_attn_timing_read(k, ctypes.byref(ms), ctypes.byref(n)), "ring_attn_timing_read")
+    return float(ms.value), int(n.value)
 
 
 def ring_attn_version() -> int:

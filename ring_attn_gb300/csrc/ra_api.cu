@@ -5,6 +5,8 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/ringattn.h"
 #include "ra_internal.h"
@@ -152,6 +154,42 @@ ra_status check_lse(const ra_tensor* t, long long b, long long h, long long s, l
 
 ra_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
 
+// ------------------------------------------------------------------ kernel timing
+// Event pairs are pooled per kernel kind and reused after each read.
+struct TimingSlot {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pool;
+  size_t used = 0;
+};
+bool g_timing_on = false;
+TimingSlot g_timing[RA_KERNEL_COUNT];
+
+// Brackets one launch with events when timing is on.
+struct TimedLaunch {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t stop = nullptr;
+  TimedLaunch(int k, cudaStream_t s) : kind(k), st(s) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_timing_on) return;
+    TimingSlot& t = g_timing[kind];
+    if (t.used == t.pool.size()) {
+      cudaEvent_t a, b;
+      if (cudaEventCreate(&a) != cudaSuccess) return;
+      if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(a);
+        return;
+      }
+      t.pool.emplace_back(a, b);
+    }
+    auto& pr = t.pool[t.used++];
+    cudaEventRecord(pr.first, st);
+    stop = pr.second;
+  }
+  ~TimedLaunch() {
+    if (stop) cudaEventRecord(stop, st);
+  }
+};
+
 #define RA_TRY(x)                    \
   do {                               \
     ra_status _s = (x);              \
@@ -198,6 +236,7 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   RA_TRY(make_tmap(q, &tq));
   RA_TRY(make_tmap(k, &tk));
   RA_TRY(make_tmap(v, &tv));
+  TimedLaunch tl(RA_KERNEL_FWD, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_fwd((int)q.d, tq, tk, tv, p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -264,8 +303,15 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(k, &tk));
   RA_TRY(make_tmap(v, &tv));
   RA_TRY(make_tmap(dout, &tdo));
-  RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, Dsum, dq_acc, st)));
-  RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, st)));
+  {
+    TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, Dsum, dq_acc, st)));
+  }
+  {
+    TimedLaunch tl(RA_KERNEL_BWD, st);
+    RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, st)));
+  }
+  TimedLaunch tl(RA_KERNEL_BWD_POST, st);
   return cuda_status(launch_bwd_post(dq_acc, vdq, st));
 }
 
@@ -382,6 +428,7 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
   a.lb_s0 = lb[0];
   a.lb_s1 = lb[1];
   a.lb_s2 = lb[2];
+  TimedLaunch tl(RA_KERNEL_LSE_MERGE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_lse_merge(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -491,6 +538,7 @@ static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t la
   a.layout = layout;
   a.N = n_shards;
   a.inverse = inverse;
+  TimedLaunch tl(RA_KERNEL_PERMUTE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -538,6 +586,30 @@ ra_status ring_attn_set_knob(int32_t knob, int64_t value) {
     return RA_OK;
   }
   return RA_ERR_INVALID_ARG;
+}
+
+ra_status ring_attn_timing_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing_on = on != 0;
+  for (auto& t : g_timing) t.used = 0;
+  return RA_OK;
+}
+
+ra_status ring_attn_timing_read(int32_t kernel, double* total_ms, int64_t* launches) {
+  if (kernel < 0 || kernel >= RA_KERNEL_COUNT || !total_ms || !launches) return RA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  TimingSlot& t = g_timing[kernel];
+  double sum = 0.0;
+  for (size_t i = 0; i < t.used; ++i) {
+    if (cudaEventSynchronize(t.pool[i].second) != cudaSuccess) return RA_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.pool[i].first, t.pool[i].second) != cudaSuccess) return RA_ERR_CUDA;
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = (int64_t)t.used;
+  t.used = 0;
+  return RA_OK;
 }
 
 const char* ra_status_string(int32_t status) {

@@ -76,7 +76,13 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
     const float A = live ? *la : 0.f;
     const float B = live ? __ldg(lb) : -INFINITY;
     __syncwarp();
-    if (!live || B == -INFINITY) continue;  // empty block: accumulator unchanged
+    if (!live) continue;
+    if (B == -INFINITY) {
+      // empty block: the accumulator is unchanged, except that an empty
+      // accumulator (lse -inf) is normalised to out = 0
+      if (A == -INFINITY) *reinterpret_cast<float4*>(oa) = make_float4(0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
     float4 ob;
     if (BLK_F32) {
       ob = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs));

@@ -25,3 +25,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _short_device_wait_limit():
+    """RA_TEST_WAIT_LIMIT_NS shortens the kernels' bounded waits for a test session."""
+    val = os.environ.get("RA_TEST_WAIT_LIMIT_NS")
+    if val:
+        try:
+            import ring_attn_gb300
+
+            ring_attn_gb300.ring_attn_set_knob(ring_attn_gb300.RA_KNOB_WAIT_LIMIT_NS, int(val))
+        except Exception:  # library not built yet: the GPU tests build it
+            pass
+    yield
