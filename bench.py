@@ -155,6 +155,22 @@ def _oracle_sample(q, k, v, do):
     return dt, 2.5 * 4.0 * n * n * D / 2.0
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest per-rank value (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flop_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's work divided by the slowest rank's time."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def _emit(obj):
     print(json.dumps(obj), flush=True)
 
@@ -288,14 +304,11 @@ def main():
     st, info = ra.ring_attn_check_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st} info {info:#x} in the timed region")
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     fwd_ms = kt["fwd"][0] / max(kt["fwd"][1], 1)
     bwd_ms = kt["bwd"][0] / max(kt["bwd"][1], 1)
-    value = world * STEP_FLOP / (ms * 1e-3) / 1e12
+    value = job_tflops(world, STEP_FLOP, ms)
     bwd_tflops = BWD_FLOP / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = FWD_FLOP / (fwd_ms * 1e-3) / 1e12
     peak_sus = peaks["bf16_sustained"]
@@ -322,7 +335,7 @@ def main():
                 "pre_ms": kt["bwd_pre"][0] / max(kt["bwd_pre"][1], 1),
                 "post_ms": kt["bwd_post"][0] / max(kt["bwd_post"][1], 1)},
         "fwd_bwd_frac_of_peak": value / world / peak_sus,
-        "fwd_bwd_tflops_3p5x": world * STEP_FLOP_ALG / (ms * 1e-3) / 1e12,
+        "fwd_bwd_tflops_3p5x": job_tflops(world, STEP_FLOP_ALG, ms),
         "roofline": roofline, "gpu_launches": launches, "clocks": clk,
         "peaks": peaks,
     }
@@ -385,13 +398,10 @@ def main():
         a1.record()
         torch.cuda.synchronize()
         e_ms = a0.elapsed_time(a1) / k_e2e
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dist, dev)
         h2d = sum(t.numel() * t.element_size() for t in hin.values())
         d2h = sum(t.numel() * t.element_size() for t in hout.values()) + hlse.numel() * 4
-        result["e2e"] = {"value": world * STEP_FLOP / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        result["e2e"] = {"value": job_tflops(world, STEP_FLOP, e_ms), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                          "steps": k_e2e, "path": "pinned host -> C-ABI permute, fwd, bwd, unpermute -> pinned host"}
 

@@ -13,7 +13,9 @@
 //     "Ring Attention + Flash Attention"; ainews.cool article "技术深度解析").
 //
 // Kernel structure (one CTA per query tile, 8 warps):
-//   warp 0     TMA producer: Q once, then K/V tiles into a 2-stage ring.
+//   warp 0     TMA producer: Q once, then K tiles into a 3-stage ring (freed
+//              when S = Q K^T completes) and V tiles into a 2-stage ring
+//              (freed when O += P V completes), so loads run ahead of use.
 //   warp 1     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
 //              tile, then O += P V into the TMEM output accumulator.
 //   warp 2     allocates / frees 512 TMEM columns.
@@ -31,15 +33,18 @@ namespace {
 
 constexpr int kBox = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 bytes) = 16 KB
 
+constexpr int kKStages = 3;  // K tiles are released as soon as S = Q K^T completes
+constexpr int kVStages = 2;  // V tiles are released when O += P V completes
+
 template <int D>
 struct FwdLayout {
   static constexpr int kTile = (D / 64) * kBox;  // one Q/K/V tile (128 rows x D)
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;          // 2 stages
-  static constexpr int kV = kK + 2 * kTile;      // 2 stages
-  static constexpr int kP = kV + 2 * kTile;      // P tile: 2 boxes (128 key columns)
+  static constexpr int kK = kQ + kTile;              // kKStages stages
+  static constexpr int kV = kK + kKStages * kTile;   // kVStages stages
+  static constexpr int kP = kV + kVStages * kTile;   // P tile: 2 boxes (128 key columns)
   static constexpr int kBar = kP + 2 * kBox;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024 bytes
@@ -48,14 +53,15 @@ struct FwdLayout {
 
 enum FwdBar {
   B_Q_FULL = 0,
-  B_K_FULL = 1,    // 2
-  B_V_FULL = 3,    // 2
-  B_KV_EMPTY = 5,  // 2
-  B_S_FULL = 7,    // 2
-  B_S_FREE = 9,    // 2
-  B_P_FULL = 11,
-  B_PV_DONE = 12,
-  B_TEARDOWN = 13
+  B_K_FULL = 1,    // kKStages
+  B_K_EMPTY = 4,   // kKStages
+  B_V_FULL = 7,    // kVStages
+  B_V_EMPTY = 9,   // kVStages
+  B_S_FULL = 11,   // 2
+  B_S_FREE = 13,   // 2
+  B_P_FULL = 15,
+  B_PV_DONE = 16,
+  B_TEARDOWN = 17
 };
 
 struct QTile {
@@ -165,14 +171,19 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q_FULL), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(BAR(B_K_FULL + i), 1);
-      mbar_init(BAR(B_V_FULL + i), 1);
-      mbar_init(BAR(B_KV_EMPTY + i), 1);
-      mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_S_FREE + i), 128);
+      mbar_init(BAR(B_K_EMPTY + i), 1);
     }
-    mbar_init(BAR(B_P_FULL), 128);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(BAR(B_V_FULL + i), 1);
+      mbar_init(BAR(B_V_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_S_FULL + i), 1);
+      mbar_init(BAR(B_S_FREE + i), 4);  // one elected arrival per softmax warp
+    }
+    mbar_init(BAR(B_P_FULL), 4);
     mbar_init(BAR(B_PV_DONE), 1);
     mbar_init(BAR(B_TEARDOWN), 1);
     *abort_flag = 0;
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_tiles > 0) {
       bool q_issued = false;
-      int n_issued[2] = {0, 0};
+      int k_issued[kKStages] = {}, v_issued[kVStages] = {};
       const int prow0 = q.r * p.L + q.i0;
       if (!(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
         mbar_expect_tx(BAR(B_Q_FULL), LY::kTile);
@@ -206,27 +217,30 @@ __global__ void __launch_bounds__(256, 1)
       }
       int j = 0;
       walk_tiles(p, q, nkt, [&](int s, int kt) {
-        const int st = j & 1;
-        if (j >= 2 && !wait_one(BAR(B_KV_EMPTY + st), ((j >> 1) - 1) & 1, abort_flag, p.ctl, 1)) return false;
+        const int ks = j % kKStages, vs = j % kVStages;
         const int row = s * p.L + kt * kTileN;
-        mbar_expect_tx(BAR(B_K_FULL + st), LY::kTile);
+        // use number u of a stage waits for the release of use u - 1
+        if (j >= kKStages && !wait_one(BAR(B_K_EMPTY + ks), (j / kKStages - 1) & 1, abort_flag, p.ctl, 1))
+          return false;
+        mbar_expect_tx(BAR(B_K_FULL + ks), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kK + st * LY::kTile + c * kBox, &tmK, BAR(B_K_FULL + st), c * 64, row, q.h, q.b);
-        mbar_expect_tx(BAR(B_V_FULL + st), LY::kTile);
+          tma_load_4d(sb + LY::kK + ks * LY::kTile + c * kBox, &tmK, BAR(B_K_FULL + ks), c * 64, row, q.h, q.b);
+        ++k_issued[ks];
+        if (j >= kVStages && !wait_one(BAR(B_V_EMPTY + vs), (j / kVStages - 1) & 1, abort_flag, p.ctl, 10))
+          return false;
+        mbar_expect_tx(BAR(B_V_FULL + vs), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kV + st * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + st), c * 64, row, q.h, q.b);
-        ++n_issued[st];
+          tma_load_4d(sb + LY::kV + vs * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + vs), c * 64, row, q.h, q.b);
+        ++v_issued[vs];
         ++j;
         return true;
       });
       // every issued copy lands before the CTA may exit
       if (q_issued) drain_one(BAR(B_Q_FULL), 0, p.ctl, 20);
-      for (int st = 0; st < 2; ++st) {
-        if (n_issued[st]) {
-          drain_one(BAR(B_K_FULL + st), (n_issued[st] - 1) & 1, p.ctl, 21);
-          drain_one(BAR(B_V_FULL + st), (n_issued[st] - 1) & 1, p.ctl, 22);
-        }
-      }
+      for (int st = 0; st < kKStages; ++st)
+        if (k_issued[st]) drain_one(BAR(B_K_FULL + st), (k_issued[st] - 1) & 1, p.ctl, 21);
+      for (int st = 0; st < kVStages; ++st)
+        if (v_issued[st]) drain_one(BAR(B_V_FULL + st), (v_issued[st] - 1) & 1, p.ctl, 22);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -236,11 +250,11 @@ __global__ void __launch_bounds__(256, 1)
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
       bool ok = wait_one(BAR(B_Q_FULL), 0, abort_flag, p.ctl, 2);
       auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
+        const int vs = i % kVStages;
         if (!wait_one(BAR(B_P_FULL), i & 1, abort_flag, p.ctl, 3)) return false;
-        if (!wait_one(BAR(B_V_FULL + st), (i >> 1) & 1, abort_flag, p.ctl, 4)) return false;
+        if (!wait_one(BAR(B_V_FULL + vs), (i / kVStages) & 1, abort_flag, p.ctl, 4)) return false;
         tc_fence_after();
-        const uint32_t vb = sb + LY::kV + st * LY::kTile;
+        const uint32_t vb = sb + LY::kV + vs * LY::kTile;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
           // A = P (K-major, 128 query rows x 128 keys); B = V (MN-major: key rows, D columns)
@@ -249,21 +263,21 @@ __global__ void __launch_bounds__(256, 1)
           mma_bf16_ss(tmem + LY::kTmemO, a, bd, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(BAR(B_PV_DONE));
-        if (i + 2 < n_tiles) mma_commit(BAR(B_KV_EMPTY + st));
+        if (i + kVStages < n_tiles) mma_commit(BAR(B_V_EMPTY + vs));
         return true;
       };
       int j = 0;
       if (ok) {
         tc_fence_after();
         walk_tiles(p, q, nkt, [&](int, int) {
-          const int st = j & 1;
-          if (!wait_one(BAR(B_K_FULL + st), (j >> 1) & 1, abort_flag, p.ctl, 5) ||
+          const int st = j & 1, ks = j % kKStages;
+          if (!wait_one(BAR(B_K_FULL + ks), (j / kKStages) & 1, abort_flag, p.ctl, 5) ||
               (j >= 2 && !wait_one(BAR(B_S_FREE + st), ((j >> 1) - 1) & 1, abort_flag, p.ctl, 6))) {
             ok = false;
             return false;
           }
           tc_fence_after();
-          const uint32_t kb = sb + LY::kK + st * LY::kTile;
+          const uint32_t kb = sb + LY::kK + ks * LY::kTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // A = Q, B = K, both K-major (D contiguous)
@@ -272,6 +286,7 @@ __global__ void __launch_bounds__(256, 1)
                         kIdS, kk > 0 ? 1u : 0u);
           }
           mma_commit(BAR(B_S_FULL + st));
+          if (j + kKStages < n_tiles) mma_commit(BAR(B_K_EMPTY + ks));
           if (j >= 1 && !issue_pv(j - 1)) {
             ok = false;
             return false;
@@ -324,14 +339,15 @@ __global__ void __launch_bounds__(256, 1)
         tmem_ld_wait(r3);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(r0[c]) * p.scale_log2;
-          x[32 + c] = __uint_as_float(r1[c]) * p.scale_log2;
-          x[64 + c] = __uint_as_float(r2[c]) * p.scale_log2;
-          x[96 + c] = __uint_as_float(r3[c]) * p.scale_log2;
+          x[c] = __uint_as_float(r0[c]);
+          x[32 + c] = __uint_as_float(r1[c]);
+          x[64 + c] = __uint_as_float(r2[c]);
+          x[96 + c] = __uint_as_float(r3[c]);
         }
       }
       tc_fence_before();
-      mbar_arrive(BAR(B_S_FREE + st));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_S_FREE + st));
       if (!tile_full(p, q, s, kt)) {
         const int j0 = kt * kTileN;
         const int jlim = min(kTileN, p.L - j0);
@@ -356,7 +372,8 @@ __global__ void __launch_bounds__(256, 1)
         m2 = fmaxf(m2, x[c + 2]);
         m3 = fmaxf(m3, x[c + 3]);
       }
-      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      // raw scores: the scale is > 0, so max(s) * scale = max(s * scale)
+      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * p.scale_log2;
       float alpha = 1.f;
       if (mx > -INFINITY) {
         if (m_run == -INFINITY) {
@@ -370,10 +387,10 @@ __global__ void __launch_bounds__(256, 1)
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int c = 0; c < kTileN; c += 4) {
-        x[c] = fast_exp2(x[c] - m_use);
-        x[c + 1] = fast_exp2(x[c + 1] - m_use);
-        x[c + 2] = fast_exp2(x[c + 2] - m_use);
-        x[c + 3] = fast_exp2(x[c + 3] - m_use);
+        x[c] = fast_exp2(fmaf(x[c], p.scale_log2, -m_use));
+        x[c + 1] = fast_exp2(fmaf(x[c + 1], p.scale_log2, -m_use));
+        x[c + 2] = fast_exp2(fmaf(x[c + 2], p.scale_log2, -m_use));
+        x[c + 3] = fast_exp2(fmaf(x[c + 3], p.scale_log2, -m_use));
         s0 += x[c];
         s1 += x[c + 1];
         s2 += x[c + 2];
@@ -412,7 +429,8 @@ __global__ void __launch_bounds__(256, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(BAR(B_P_FULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL));
       ++j;
       return true;
     });
