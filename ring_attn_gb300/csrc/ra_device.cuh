@@ -71,7 +71,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // One thread waits.  Returns false when the CTA aborts (own timeout or another role's).
-static __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
+static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
                                       int site) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer();
@@ -89,7 +89,7 @@ static __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, vola
 }
 
 // A whole converged warp waits; the result is the same on every lane.
-static __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
+static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
                                        int site) {
   unsigned long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
@@ -114,6 +114,19 @@ static __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, vol
       if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
   }
+}
+
+// Per-warpgroup register budgets (all four warps of a warpgroup execute these).
+// The sum over warpgroups must not exceed the block's launch allocation, or
+// setmaxnreg.inc would wait forever: launchers check the kernel's register
+// count before using a split.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Named barrier among a subset of warps (ids 1..15; 0 is __syncthreads).
@@ -168,6 +181,19 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, fp32 accumulate.  A (M x K,
+// K-major) sits in tensor memory: row m in lane m, two consecutive bf16 K
+// elements per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -237,6 +263,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Lane (32*quadrant + laneid) writes 16 consecutive 32-bit columns starting at taddr's column.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      RA_I8(0), RA_I8(8)
+      : "memory");
+}
+
 #undef RA_R8
 #undef RA_P8
 #undef RA_I8
@@ -254,49 +289,50 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ------------------------------------------------------------------ layouts
 // Original token index of local position i in shard r (L tokens per shard).
+// 32-bit: the host validates s <= 2^30, so every token index fits.
 enum : int { LAYOUT_CONTIGUOUS = 0, LAYOUT_ZIGZAG = 1, LAYOUT_STRIPE = 2 };
 
-__host__ __device__ __forceinline__ long long token_of(int layout, int N, int L, int r, int i) {
-  if (layout == LAYOUT_STRIPE) return (long long)i * N + r;
+__host__ __device__ __forceinline__ int token_of(int layout, int N, int L, int r, int i) {
+  if (layout == LAYOUT_STRIPE) return i * N + r;
   if (layout == LAYOUT_ZIGZAG) {
-    int c = L >> 1;
-    return i < c ? (long long)r * c + i : (long long)(2 * N - 1 - r) * c + (i - c);
+    const int c = L >> 1;
+    return i < c ? r * c + i : (2 * N - 1 - r) * c + (i - c);
   }
-  return (long long)r * L + i;
+  return r * L + i;
 }
 
 // Largest local index j of shard s with token_of(s, j) <= g, or -1.
-__host__ __device__ __forceinline__ int last_local_at_or_before(int layout, int N, int L, int s, long long g) {
+__host__ __device__ __forceinline__ int last_local_at_or_before(int layout, int N, int L, int s, int g) {
   if (layout == LAYOUT_STRIPE) {
     if (g < s) return -1;
-    long long j = (g - s) / N;
-    return (int)(j < L - 1 ? j : L - 1);
+    const int j = (g - s) / N;
+    return j < L - 1 ? j : L - 1;
   }
   if (layout == LAYOUT_ZIGZAG) {
-    int c = L >> 1;
-    long long hi0 = (long long)(2 * N - 1 - s) * c;
+    const int c = L >> 1;
+    const int hi0 = (2 * N - 1 - s) * c;
     if (g >= hi0) {
-      long long j = c + (g - hi0);
-      return (int)(j < L - 1 ? j : L - 1);
+      const int j = c + (g - hi0);
+      return j < L - 1 ? j : L - 1;
     }
-    long long lo0 = (long long)s * c;
+    const int lo0 = s * c;
     if (g >= lo0) {
-      long long j = g - lo0;
-      return (int)(j < c - 1 ? j : c - 1);
+      const int j = g - lo0;
+      return j < c - 1 ? j : c - 1;
     }
     return -1;
   }
-  long long j = g - (long long)s * L;
+  const int j = g - s * L;
   if (j < 0) return -1;
-  return (int)(j < L - 1 ? j : L - 1);
+  return j < L - 1 ? j : L - 1;
 }
 
 // Segment index k with cu[k] <= t < cu[k+1] (binary search, n_seqs >= 1).
-__device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs, long long t) {
+__device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs, int t) {
   int lo = 0, hi = n_seqs - 1;
   while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if ((long long)__ldg(cu + mid) <= t)
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t)
       lo = mid;
     else
       hi = mid - 1;
@@ -309,7 +345,7 @@ __device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs
 namespace ra {
 // Wait that ignores the abort flag (bounded by time only): used at teardown to
 // let copies and MMAs already in flight land before the CTA exits.
-static __device__ __noinline__ void drain_one(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
+static __device__ __forceinline__ void drain_one(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
   unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > c.wait_limit_ns) {

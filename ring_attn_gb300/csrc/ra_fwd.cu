@@ -1,6 +1,6 @@
-// Ring-attention forward on sm_103a: blockwise exact attention of one 128-row
-// query tile against every key tile of the KV shards it meets on the ring,
-// with the online-softmax merge held in fp32 across all ring steps.
+// Ring-attention forward on sm_103a: blockwise exact attention of query tiles
+// against every key tile of the KV shards they meet on the ring, with the
+// online-softmax merge held in fp32 across all ring steps.
 //
 // Method (cited by page title and section):
 //   * ring order: at step t the Q shard r meets KV shard (r - t) mod N
@@ -12,43 +12,62 @@
 //   * tiles of 128 tokens, scores never materialised in HBM (same page,
 //     "Ring Attention + Flash Attention"; ainews.cool article "技术深度解析").
 //
-// Kernel structure (one CTA per query tile, 8 warps):
-//   warp 0     TMA producer: Q once, then K tiles into a 3-stage ring (freed
-//              when S = Q K^T completes) and V tiles into a 2-stage ring
-//              (freed when O += P V completes), so loads run ahead of use.
-//   warp 1     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
-//              tile, then O += P V into the TMEM output accumulator.
-//   warp 2     allocates / frees 512 TMEM columns.
-//   warps 4-7  softmax: one thread per query row (the TMEM lane of that row).
-//              It reads its S row from TMEM, masks, updates the running max
-//              (rescaling O only when the max grows by more than 2^8), writes
-//              P as bf16 into a 128B-swizzled shared tile for the PV MMA, and
-//              finally normalises O and writes out and lse.
-// Empty key tiles (causal / varlen) are never loaded; only partial tiles are
-// masked element by element.
+// Kernel structure: one CTA owns two 128-row query tiles (Q0, Q1: 256
+// consecutive rows of one shard) and 12 warps.
+//   warps 0, 3  TMA producers: warp 0 loads Q0 and Q1 once, then K tiles into a
+//               3-stage ring (freed when both S MMAs of a tile complete); warp 3
+//               loads V tiles into a 2-stage ring (freed when both PV MMAs
+//               complete), so K loads are never held back by the V ring.
+//   warp 1      MMA issuer (one thread).  Per key tile j it issues
+//                 PV0(j-1), S0(j), PV1(j-1), S1(j)
+//               (PV0(j-1) does not wait for K(j)),
+//               so the tensor core works on one query tile while the other
+//               tile's softmax runs (ping-pong).  S_t = Q_t K^T lands in TMEM
+//               columns [128 t, 128 t + 128); O_t in [256 + 128 t, ...).
+//   warp 2      allocates / frees the 512 TMEM columns.
+//   warps 4-7   softmax of Q0, warps 8-11 softmax of Q1: one thread per query
+//               row (its TMEM lane).  A thread reads its 128 scores, masks
+//               partial tiles, updates the running max (O is rescaled in TMEM
+//               only when the max grows by more than 2^8), and writes P as
+//               packed bf16 over the first 64 columns of its own S tile, which
+//               the PV MMA then reads as its A operand straight from TMEM.
+// The commit that signals S_t(j) also covers PV_t(j-1) (commits track every
+// earlier MMA of the issuing thread), so a softmax thread may rescale O_t as
+// soon as its S tile is ready.  Empty key tiles are never loaded; only
+// partial tiles are masked element by element.
 #include "ra_internal.h"
 
 namespace ra {
 namespace {
 
 constexpr int kBox = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 bytes) = 16 KB
-
-constexpr int kKStages = 3;  // K tiles are released as soon as S = Q K^T completes
-constexpr int kVStages = 2;  // V tiles are released when O += P V completes
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kQTiles = 2;       // query tiles per CTA
+constexpr int kRowsPerCta = kQTiles * kTileM;
+constexpr int kThreads = 384;
+// Register split: the producer / MMA warpgroup gives registers to the two
+// softmax warpgroups, which hold a whole 128-score row each.  The launch
+// allocation is kThreads * kLaunchRegs, and 128 * kRegsLow + 256 * kRegsHigh
+// must not exceed it (checked by the launcher against the compiled kernel).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 72;
+constexpr int kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split exceeds the launch");
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kTile = (D / 64) * kBox;  // one Q/K/V tile (128 rows x D)
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;              // kKStages stages
+  static constexpr int kTile = (D / 64) * kBox;      // one Q/K/V tile (128 rows x D)
+  static constexpr int kQ = 0;                       // Q0, Q1
+  static constexpr int kK = kQ + kQTiles * kTile;    // kKStages stages
   static constexpr int kV = kK + kKStages * kTile;   // kVStages stages
-  static constexpr int kP = kV + kVStages * kTile;   // P tile: 2 boxes (128 key columns)
-  static constexpr int kBar = kP + 2 * kBox;
-  static constexpr int kNumBars = 18;
+  static constexpr int kBar = kV + kVStages * kTile;
+  static constexpr int kNumBars = 17;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024 bytes
-  static constexpr uint32_t kTmemO = 256;        // S buffers at columns 0 and 128
+  static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024 bytes
+  static constexpr uint32_t kTmemS = 0;              // + 128 t
+  static constexpr uint32_t kTmemO = 256;            // + 128 t
 };
 
 enum FwdBar {
@@ -57,33 +76,51 @@ enum FwdBar {
   B_K_EMPTY = 4,   // kKStages
   B_V_FULL = 7,    // kVStages
   B_V_EMPTY = 9,   // kVStages
-  B_S_FULL = 11,   // 2
-  B_S_FREE = 13,   // 2
-  B_P_FULL = 15,
-  B_PV_DONE = 16,
-  B_TEARDOWN = 17
+  B_S_FULL = 11,   // kQTiles
+  B_P_FULL = 13,   // kQTiles
+  B_O_DONE = 15,
+  B_TEARDOWN = 16
 };
 
-struct QTile {
-  int b, h, r, i0, i_last;
-  long long gq_lo, gq_hi;    // original token indices of the first / last valid row
-  long long key_lo, key_hi;  // varlen: keys any row of the tile may see (inclusive)
+// Rows [i0, i0 + rows) of Q shard r; the valid ones end at i_last.
+struct QRange {
+  int r, i0, i_last;
+  int gq_lo, gq_hi;    // original token indices of the first / last valid row
+  int key_lo, key_hi;  // varlen: keys any row may see (inclusive)
   int seg_single;            // varlen: the segment of every valid row, or -1
 };
 
-// Key-tile range [lo, hi) of KV shard s that can hold an allowed key.
-__device__ __forceinline__ void kv_range(const FwdParams& p, const QTile& q, int s, int nkt, int& lo, int& hi) {
+__device__ __forceinline__ void make_range(const FwdParams& p, int r, int i0, int rows, QRange& q) {
+  q.r = r;
+  q.i0 = i0;
+  q.i_last = min(i0 + rows, p.L) - 1;
+  const int ilo = min(i0, p.L - 1);
+  q.gq_lo = token_of(p.layout, p.N, p.L, r, ilo);
+  q.gq_hi = token_of(p.layout, p.N, p.L, r, max(q.i_last, ilo));
+  q.key_lo = q.key_hi = 0;
+  q.seg_single = -1;
   if (p.cu) {
-    const long long base = (long long)s * p.L;
-    long long jlo = q.key_lo - base, jhi = q.key_hi - base;
+    const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
+    const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
+    q.key_lo = __ldg(p.cu + sa);
+    q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
+    q.seg_single = sa == sz ? sa : -1;
+  }
+}
+
+// Key-tile range [lo, hi) of KV shard s that can hold a key allowed for some row of q.
+__device__ __forceinline__ void kv_range(const FwdParams& p, const QRange& q, int s, int nkt, int& lo, int& hi) {
+  if (p.cu) {
+    const int base = s * p.L;
+    int jlo = q.key_lo - base, jhi = q.key_hi - base;
     if (jlo < 0) jlo = 0;
     if (jhi > p.L - 1) jhi = p.L - 1;
     if (jlo > jhi) {
       lo = hi = 0;
       return;
     }
-    lo = (int)(jlo / kTileN);
-    hi = (int)(jhi / kTileN) + 1;
+    lo = jlo / kTileN;
+    hi = jhi / kTileN + 1;
     return;
   }
   lo = 0;
@@ -91,29 +128,29 @@ __device__ __forceinline__ void kv_range(const FwdParams& p, const QTile& q, int
     hi = nkt;
     return;
   }
-  // token_of is increasing inside a shard, so the allowed keys of the tile's
-  // last (largest-token) row are a prefix of the shard.
+  // token_of is increasing inside a shard, so the allowed keys of the largest
+  // row token are a prefix of the shard and cover every other row's keys.
   const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, q.gq_hi);
   hi = jm < 0 ? 0 : jm / kTileN + 1;
 }
 
-// True when every (valid row, key) pair of the tile is allowed: no masking needed.
-__device__ __forceinline__ bool tile_full(const FwdParams& p, const QTile& q, int s, int kt) {
+// True when every (valid row of q, key) pair of the tile is allowed: no masking needed.
+__device__ __forceinline__ bool tile_full(const FwdParams& p, const QRange& q, int s, int kt) {
   const int j0 = kt * kTileN;
-  if (j0 + kTileN > p.L) return false;
+  if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
   if (p.cu) {
     if (q.seg_single < 0) return false;
-    const long long base = (long long)s * p.L + j0;
-    const long long slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
+    const int base = s * p.L + j0;
+    const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
     if (base < slo || base + kTileN > shi) return false;
     return !p.causal || q.gq_lo >= base + kTileN - 1;
   }
   return !p.causal || q.gq_lo >= token_of(p.layout, p.N, p.L, s, j0 + kTileN - 1);
 }
 
-// Calls f(s, kt) for every key tile the query tile meets, in ring order.
+// Calls f(s, kt) for every key tile the CTA's rows meet, in ring order.
 template <class F>
-__device__ __forceinline__ void walk_tiles(const FwdParams& p, const QTile& q, int nkt, F&& f) {
+__device__ __forceinline__ void walk_tiles(const FwdParams& p, const QRange& q, int nkt, F&& f) {
   const int t0 = p.step < 0 ? 0 : p.step;
   const int t1 = p.step < 0 ? p.N : p.step + 1;
   for (int t = t0; t < t1; ++t) {
@@ -127,7 +164,7 @@ __device__ __forceinline__ void walk_tiles(const FwdParams& p, const QTile& q, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     ring_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using LY = FwdLayout<D>;
@@ -138,28 +175,18 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  QTile q;
-  q.b = blockIdx.y / p.H;
-  q.h = blockIdx.y % p.H;
-  // causal: the later query tiles carry more work, start them first
+  const int b = blockIdx.y / p.H;
+  const int h = blockIdx.y % p.H;
+  // causal: the later query rows carry more work, start them first
   const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  q.r = x / p.n_qtiles;
-  q.i0 = (x % p.n_qtiles) * kTileM;
-  q.i_last = min(q.i0 + kTileM, p.L) - 1;
-  q.gq_lo = token_of(p.layout, p.N, p.L, q.r, q.i0);
-  q.gq_hi = token_of(p.layout, p.N, p.L, q.r, q.i_last);
-  q.key_lo = q.key_hi = 0;
-  q.seg_single = -1;
-  if (p.cu) {
-    const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
-    const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
-    q.key_lo = __ldg(p.cu + sa);
-    q.key_hi = p.causal ? q.gq_hi : (long long)__ldg(p.cu + sz + 1) - 1;
-    q.seg_single = sa == sz ? sa : -1;
-  }
+  const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
+  const int r = x / n_pairs;
+  const int i0 = (x % n_pairs) * kRowsPerCta;
+  QRange cta;  // both query tiles together: decides which key tiles are visited
+  make_range(p, r, i0, kRowsPerCta, cta);
   const int nkt = (p.L + kTileN - 1) / kTileN;
   int n_tiles = 0;
-  walk_tiles(p, q, nkt, [&](int, int) {
+  walk_tiles(p, cta, nkt, [&](int, int) {
     ++n_tiles;
     return true;
   });
@@ -179,12 +206,11 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(BAR(B_V_FULL + i), 1);
       mbar_init(BAR(B_V_EMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_S_FREE + i), 4);  // one elected arrival per softmax warp
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(BAR(B_S_FULL + t), 1);
+      mbar_init(BAR(B_P_FULL + t), 4);  // one elected arrival per softmax warp
     }
-    mbar_init(BAR(B_P_FULL), 4);
-    mbar_init(BAR(B_PV_DONE), 1);
+    mbar_init(BAR(B_O_DONE), 1);
     mbar_init(BAR(B_TEARDOWN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -202,178 +228,186 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp < 4) {
+    // ------------------------------------------------------------ control warpgroup
+    regs_dec<kRegsLow>();
+    if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0 loads Q and the K ring, warp 3 the V ring: K tiles run ahead of
+    // the V ring, which frees a stage only once both PV MMAs of a tile are done
     if (lane == 0 && n_tiles > 0) {
+      const bool is_k = warp == 0;
       bool q_issued = false;
-      int k_issued[kKStages] = {}, v_issued[kVStages] = {};
-      const int prow0 = q.r * p.L + q.i0;
-      if (!(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
-        mbar_expect_tx(BAR(B_Q_FULL), LY::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0, q.h, q.b);
+      int issued[kKStages] = {};
+      const int nst = is_k ? kKStages : kVStages;
+      const int full0 = is_k ? B_K_FULL : B_V_FULL, empty0 = is_k ? B_K_EMPTY : B_V_EMPTY;
+      const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
+      const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+      if (is_k && !(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
+        const int prow0 = r * p.L + i0;
+        mbar_expect_tx(BAR(B_Q_FULL), kQTiles * LY::kTile);
+        for (int t = 0; t < kQTiles; ++t)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + LY::kQ + t * LY::kTile + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0 + t * kTileM,
+                        h, b);
         q_issued = true;
       }
       int j = 0;
-      walk_tiles(p, q, nkt, [&](int s, int kt) {
-        const int ks = j % kKStages, vs = j % kVStages;
-        const int row = s * p.L + kt * kTileN;
-        // use number u of a stage waits for the release of use u - 1
-        if (j >= kKStages && !wait_one(BAR(B_K_EMPTY + ks), (j / kKStages - 1) & 1, abort_flag, p.ctl, 1))
+      walk_tiles(p, cta, nkt, [&](int s, int kt) {
+        const int st = j % nst;
+        // use u of a stage waits for the release of use u - 1
+        if (j >= nst && !wait_one(BAR(empty0 + st), (j / nst - 1) & 1, abort_flag, p.ctl, is_k ? 1 : 10))
           return false;
-        mbar_expect_tx(BAR(B_K_FULL + ks), LY::kTile);
+        mbar_expect_tx(BAR(full0 + st), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kK + ks * LY::kTile + c * kBox, &tmK, BAR(B_K_FULL + ks), c * 64, row, q.h, q.b);
-        ++k_issued[ks];
-        if (j >= kVStages && !wait_one(BAR(B_V_EMPTY + vs), (j / kVStages - 1) & 1, abort_flag, p.ctl, 10))
-          return false;
-        mbar_expect_tx(BAR(B_V_FULL + vs), LY::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kV + vs * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + vs), c * 64, row, q.h, q.b);
-        ++v_issued[vs];
+          tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
+        ++issued[st];
         ++j;
         return true;
       });
       // every issued copy lands before the CTA may exit
       if (q_issued) drain_one(BAR(B_Q_FULL), 0, p.ctl, 20);
-      for (int st = 0; st < kKStages; ++st)
-        if (k_issued[st]) drain_one(BAR(B_K_FULL + st), (k_issued[st] - 1) & 1, p.ctl, 21);
-      for (int st = 0; st < kVStages; ++st)
-        if (v_issued[st]) drain_one(BAR(B_V_FULL + st), (v_issued[st] - 1) & 1, p.ctl, 22);
+      for (int st = 0; st < nst; ++st)
+        if (issued[st]) drain_one(BAR(full0 + st), (issued[st] - 1) & 1, p.ctl, 21);
     }
     __syncwarp();
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTileN, 0, 0);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTileN, 0, 0);  // A = Q, B = K: both K-major
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V: MN-major
       bool ok = wait_one(BAR(B_Q_FULL), 0, abort_flag, p.ctl, 2);
-      auto issue_pv = [&](int i) -> bool {
-        const int vs = i % kVStages;
-        if (!wait_one(BAR(B_P_FULL), i & 1, abort_flag, p.ctl, 3)) return false;
-        if (!wait_one(BAR(B_V_FULL + vs), (i / kVStages) & 1, abort_flag, p.ctl, 4)) return false;
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kb = sb + LY::kK + (j % kKStages) * LY::kTile;
+        const uint32_t qb = sb + LY::kQ + t * LY::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_bf16_ss(tmem + LY::kTmemS + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                      kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(BAR(B_S_FULL + t));
+      };
+      auto issue_pv = [&](int t, int i) -> bool {
+        if (!wait_one(BAR(B_P_FULL + t), i & 1, abort_flag, p.ctl, 3)) return false;
+        if (t == 0 && !wait_one(BAR(B_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.ctl, 4)) return false;
         tc_fence_after();
-        const uint32_t vb = sb + LY::kV + vs * LY::kTile;
+        const uint32_t vb = sb + LY::kV + (i % kVStages) * LY::kTile;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // A = P (K-major, 128 query rows x 128 keys); B = V (MN-major: key rows, D columns)
-          const uint64_t a = sdesc_sw128(sb + LY::kP + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kBox, 1024);
-          mma_bf16_ss(tmem + LY::kTmemO, a, bd, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+          // A = P: 16 keys = 8 packed columns of the S_t tile; B = V: 16 key rows = 2048 bytes
+          mma_bf16_ts(tmem + LY::kTmemO + t * 128, tmem + LY::kTmemS + t * 128 + kk * 8,
+                      sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(BAR(B_PV_DONE));
-        if (i + kVStages < n_tiles) mma_commit(BAR(B_V_EMPTY + vs));
+        if (t == kQTiles - 1 && i + kVStages < n_tiles) mma_commit(BAR(B_V_EMPTY + i % kVStages));
         return true;
       };
       int j = 0;
       if (ok) {
         tc_fence_after();
-        walk_tiles(p, q, nkt, [&](int, int) {
-          const int st = j & 1, ks = j % kKStages;
-          if (!wait_one(BAR(B_K_FULL + ks), (j / kKStages) & 1, abort_flag, p.ctl, 5) ||
-              (j >= 2 && !wait_one(BAR(B_S_FREE + st), ((j >> 1) - 1) & 1, abort_flag, p.ctl, 6))) {
-            ok = false;
-            return false;
+        walk_tiles(p, cta, nkt, [&](int, int) {
+          for (int t = 0; t < kQTiles; ++t) {
+            // PV_t(j-1) reads P_t from the S_t columns, so it goes first; S_t(j) then overwrites them
+            if (j >= 1 && !issue_pv(t, j - 1)) {
+              ok = false;
+              return false;
+            }
+            if (t == 0) {
+              if (!wait_one(BAR(B_K_FULL + j % kKStages), (j / kKStages) & 1, abort_flag, p.ctl, 5)) {
+                ok = false;
+                return false;
+              }
+              tc_fence_after();
+            }
+            issue_s(t, j);
           }
-          tc_fence_after();
-          const uint32_t kb = sb + LY::kK + ks * LY::kTile;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // A = Q, B = K, both K-major (D contiguous)
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + st * 128, sdesc_sw128(sb + LY::kQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                        kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(BAR(B_S_FULL + st));
-          if (j + kKStages < n_tiles) mma_commit(BAR(B_K_EMPTY + ks));
-          if (j >= 1 && !issue_pv(j - 1)) {
-            ok = false;
-            return false;
-          }
+          if (j + kKStages < n_tiles) mma_commit(BAR(B_K_EMPTY + j % kKStages));
           ++j;
           return true;
         });
-        if (ok && j >= 1) issue_pv(j - 1);
+        if (ok && j >= 1)
+          for (int t = 0; t < kQTiles && ok; ++t) ok = issue_pv(t, j - 1);
+        if (ok) mma_commit(BAR(B_O_DONE));
       }
       // every issued MMA completes before the CTA frees TMEM
       mma_commit(BAR(B_TEARDOWN));
       drain_one(BAR(B_TEARDOWN), 0, p.ctl, 23);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+    }
+  } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int row = (warp - 4) * 32 + lane;
+    regs_inc<kRegsHigh>();
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int row = ((warp - 4) & 3) * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int i = q.i0 + row;
+    const uint32_t tS = tl + LY::kTmemS + t * 128;
+    const uint32_t tO = tl + LY::kTmemO + t * 128;
+    QRange qt;
+    make_range(p, r, i0 + t * kTileM, kTileM, qt);
+    const int i = i0 + t * kTileM + row;
     const bool valid = i < p.L;
-    const long long gq = token_of(p.layout, p.N, p.L, q.r, valid ? i : q.i_last);
-    long long rk_lo = 0, rk_hi = 0;  // varlen: this row's allowed keys [rk_lo, rk_hi)
+    const int gq = token_of(p.layout, p.N, p.L, r, valid ? i : max(qt.i_last, 0));
+    int rk_lo = 0, rk_hi = 0;  // varlen: this row's allowed keys [rk_lo, rk_hi)
     if (p.cu) {
       const int sg = segment_of(p.cu, p.n_seqs, gq);
       rk_lo = __ldg(p.cu + sg);
-      rk_hi = p.causal ? gq + 1 : (long long)__ldg(p.cu + sg + 1);
+      rk_hi = p.causal ? gq + 1 : __ldg(p.cu + sg + 1);
     }
     float m_run = -INFINITY;  // running max, in log2 units (scores * scale * log2 e)
     float l_run = 0.f;        // running sum of exp2(x - m_run)
     bool ok = true;
     int j = 0;
-    walk_tiles(p, q, nkt, [&](int s, int kt) {
-      const int st = j & 1;
-      if (!wait_warp(BAR(B_S_FULL + st), (j >> 1) & 1, abort_flag, p.ctl, 7)) {
+    walk_tiles(p, cta, nkt, [&](int s, int kt) {
+      if (!wait_warp(BAR(B_S_FULL + t), j & 1, abort_flag, p.ctl, 7)) {
         ok = false;
         return false;
       }
       tc_fence_after();
-      float x[kTileN];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        const uint32_t sa = tl + (uint32_t)(st * 128);
-        tmem_ld32(sa + 0, r0);
-        tmem_ld32(sa + 32, r1);
-        tmem_ld32(sa + 64, r2);
-        tmem_ld32(sa + 96, r3);
-        tmem_ld_wait(r0);
-        tmem_ld_wait(r1);
-        tmem_ld_wait(r2);
-        tmem_ld_wait(r3);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(r0[c]);
-          x[32 + c] = __uint_as_float(r1[c]);
-          x[64 + c] = __uint_as_float(r2[c]);
-          x[96 + c] = __uint_as_float(r3[c]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_S_FREE + st));
-      if (!tile_full(p, q, s, kt)) {
+      // column window [c_lo, c_hi) of allowed keys for this row (all 128 when the tile is full)
+      int c_lo = 0, c_hi = kTileN;
+      if (!tile_full(p, qt, s, kt)) {
         const int j0 = kt * kTileN;
         const int jlim = min(kTileN, p.L - j0);
-        int c_lo = 0, c_hi = jlim;
+        c_hi = jlim;
         if (p.cu) {
-          const long long base = (long long)s * p.L + j0;
-          const long long lo = rk_lo - base, hi = rk_hi - base;
-          c_lo = (int)(lo < 0 ? 0 : (lo > kTileN ? kTileN : lo));
-          c_hi = (int)(hi < 0 ? 0 : (hi > jlim ? jlim : hi));
+          const int base = s * p.L + j0;
+          const int lo = rk_lo - base, hi = rk_hi - base;
+          c_lo = lo < 0 ? 0 : (lo > kTileN ? kTileN : lo);
+          c_hi = hi < 0 ? 0 : (hi > jlim ? jlim : hi);
         } else if (p.causal) {
           const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, gq);
           c_hi = min(jlim, jm - j0 + 1);
         }
-#pragma unroll
-        for (int c = 0; c < kTileN; ++c) x[c] = (c >= c_lo && c < c_hi) ? x[c] : -INFINITY;
       }
-      float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+      const bool masked = c_lo > 0 || c_hi < kTileN;
+      // all 128 scores of the row in registers: four loads, one wait
+      uint32_t v[kTileN];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 0));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : __float_as_uint(-INFINITY);
+      }
+      float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+      float m2 = __uint_as_float(v[2]), m3 = __uint_as_float(v[3]);
 #pragma unroll
       for (int c = 4; c < kTileN; c += 4) {
-        m0 = fmaxf(m0, x[c]);
-        m1 = fmaxf(m1, x[c + 1]);
-        m2 = fmaxf(m2, x[c + 2]);
-        m3 = fmaxf(m3, x[c + 3]);
+        m0 = fmaxf(m0, __uint_as_float(v[c]));
+        m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+        m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+        m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
       }
+      m0 = fmaxf(m0, m2);
+      m1 = fmaxf(m1, m3);
       // raw scores: the scale is > 0, so max(s) * scale = max(s * scale)
-      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * p.scale_log2;
+      const float mx = fmaxf(m0, m1) * p.scale_log2;
       float alpha = 1.f;
       if (mx > -INFINITY) {
         if (m_run == -INFINITY) {
@@ -384,67 +418,55 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      // P = exp2(s * scale - m) and the row sum; P goes as bf16 pairs over the
+      // first 64 columns of this tile's S columns (column 16 c32 + u holds keys
+      // 32 c32 + 2u and 32 c32 + 2u + 1); the scores are already in registers.
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < kTileN; c += 4) {
-        x[c] = fast_exp2(fmaf(x[c], p.scale_log2, -m_use));
-        x[c + 1] = fast_exp2(fmaf(x[c + 1], p.scale_log2, -m_use));
-        x[c + 2] = fast_exp2(fmaf(x[c + 2], p.scale_log2, -m_use));
-        x[c + 3] = fast_exp2(fmaf(x[c + 3], p.scale_log2, -m_use));
-        s0 += x[c];
-        s1 += x[c + 1];
-        s2 += x[c + 2];
-        s3 += x[c + 3];
-      }
-      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
-      if (j > 0) {
-        // the previous PV has finished: P's buffer is free and O is stable
-        if (!wait_warp(BAR(B_PV_DONE), (j - 1) & 1, abort_flag, p.ctl, 8)) {
-          ok = false;
-          return false;
+      for (int c32 = 0; c32 < kTileN / 32; ++c32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float e0 = fast_exp2(fmaf(__uint_as_float(v[c32 * 32 + 2 * u]), p.scale_log2, -m_use));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(v[c32 * 32 + 2 * u + 1]), p.scale_log2, -m_use));
+          s0 += e0;
+          s1 += e1;
+          pk[u] = pack_bf16x2(e0, e1);
         }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        tmem_st16(tS + c32 * 16, pk);
+      }
+      l_run = l_run * alpha + (s0 + s1);
+      // O_t is stable here (the commit behind S_FULL covers PV_t(j-1)) and PV_t(j)
+      // waits for P_FULL, so the rescale fits between them
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tl + LY::kTmemO + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(tl + LY::kTmemO + c * 32, o);
-          }
-          tmem_st_wait();
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(tO + c * 32, o);
         }
       }
-      uint8_t* pb = sp + LY::kP;
-#pragma unroll
-      for (int k = 0; k < kTileN / 8; ++k) {
-        uint4 v;
-        v.x = pack_bf16x2(x[8 * k + 0], x[8 * k + 1]);
-        v.y = pack_bf16x2(x[8 * k + 2], x[8 * k + 3]);
-        v.z = pack_bf16x2(x[8 * k + 4], x[8 * k + 5]);
-        v.w = pack_bf16x2(x[8 * k + 6], x[8 * k + 7]);
-        *reinterpret_cast<uint4*>(pb + (k >> 3) * kBox + sw128_offset(row, k & 7)) = v;
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_P_FULL));
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL + t));
       ++j;
       return true;
     });
 
-    const long long orow = (long long)q.b * p.o_sb + (long long)q.h * p.o_sh + (long long)(q.r * p.L + i) * p.o_ss;
-    float* lse_ptr = p.lse + (long long)q.b * p.l_sb + (long long)q.h * p.l_sh + (long long)(q.r * p.L + i) * p.l_ss;
+    const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(r * p.L + i) * p.o_ss;
+    float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + (long long)(r * p.L + i) * p.l_ss;
     if (n_tiles > 0) {
-      if (ok && wait_warp(BAR(B_PV_DONE), (n_tiles - 1) & 1, abort_flag, p.ctl, 9)) {
+      if (ok && wait_warp(BAR(B_O_DONE), 0, abort_flag, p.ctl, 9)) {
         tc_fence_after();
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(tl + LY::kTmemO + c * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
           if (valid) {
             if (p.out_f32) {
@@ -495,10 +517,17 @@ template <int D>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                          cudaStream_t st) {
   using LY = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(ring_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
+  // the register split inside the kernel is only safe with the launch
+  // allocation it was sized for
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, ring_fwd_kernel<D>);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(p.N * p.n_qtiles), (unsigned)(p.B * p.H));
-  ring_fwd_kernel<D><<<grid, 256, LY::kAlloc, st>>>(tq, tk, tv, p);
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(ring_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
+  dim3 grid((unsigned)(p.N * n_pairs), (unsigned)(p.B * p.H));
+  ring_fwd_kernel<D><<<grid, kThreads, LY::kAlloc, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
