@@ -268,7 +268,7 @@ def main():
     out = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(ra.ring_attn_workspace_size(1, B, H, S, D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(ra.ring_attn_workspace_size(1, B, H, S, D, N_SHARDS), dtype=torch.uint8, device=dev)
 
     def step():
         ra.ring_attn_fwd(q, k, v, LAYOUT, N_SHARDS, True, scale, out=out, lse=lse)

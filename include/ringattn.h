@@ -125,7 +125,7 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
  *   D = rowsum(dO * O), dV = P^T dO, dS = P * (dO V^T - D), dQ = scale dS K,
  *   dK = scale dS^T Q.  dK and dV stay tile-local in tensor memory; dQ is
  *   accumulated in fp32 in the workspace and cast at the end.
- *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d) bytes,
+ *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards) bytes,
  *   256-byte aligned, owned by the caller, contents need not be initialised. */
 ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                         const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
@@ -164,9 +164,12 @@ ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, in
 ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,
                               void* stream);
 
-/* Workspace bytes needed by `op` (ra_op) for (b, h, s, d); 0 for RA_OP_FWD.
- * RA_OP_BWD: an fp32 dQ accumulator (b*h*s*d) and D = rowsum(dO*O) (b*h*s). */
-size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d);
+/* Workspace bytes needed by `op` (ra_op) for (b, h, s, d) split into n_shards
+ * shards; 0 for RA_OP_FWD.  RA_OP_BWD: an fp32 dQ accumulator (b*h*s*d), then
+ * D = rowsum(dO*O) and lse*log2(e) per query row, each laid out per shard with
+ * the shard's rows padded to a multiple of 128 (b*h*n_shards*ceil(s/n_shards/128)*128
+ * floats each); every part 256-byte aligned.  Varlen calls use b = 1, s = total. */
+size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards);
 
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns RA_OK, RA_ERR_TIMEOUT (a bounded wait ran out: the kernel gave up

@@ -84,7 +84,7 @@ def load():
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = I32
-    lib.ring_attn_workspace_size.argtypes = [I32, I64, I64, I64, I64]
+    lib.ring_attn_workspace_size.argtypes = [I32, I64, I64, I64, I64, I32]
     lib.ring_attn_workspace_size.restype = SZ
     lib.ra_status_string.argtypes = [I32]
     lib.ra_status_string.restype = ctypes.c_char_p
@@ -182,8 +182,8 @@ def lse_merge(out_acc, lse_acc, out_blk, lse_blk, stream=None):
     return out_acc, lse_acc
 
 
-def ring_attn_workspace_size(op, b, h, s, d) -> int:
-    return int(load().ring_attn_workspace_size(int(op), int(b), int(h), int(s), int(d)))
+def ring_attn_workspace_size(op, b, h, s, d, n_shards=1) -> int:
+    return int(load().ring_attn_workspace_size(int(op), int(b), int(h), int(s), int(d), int(n_shards)))
 
 
 def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
@@ -194,7 +194,7 @@ def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, caus
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, b, h, s, d)
+    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
@@ -251,7 +251,7 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, 1, h, total, d)
+    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, 1, h, total, d, n_shards)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]

@@ -240,10 +240,17 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   return cuda_status(launch_fwd((int)q.d, tq, tk, tv, p, static_cast<cudaStream_t>(stream)));
 }
 
-size_t bwd_ws_bytes(long long b, long long h, long long s, long long d) {
-  const size_t acc = (size_t)b * h * s * d * sizeof(float);
-  const size_t acc_al = (acc + 255) & ~(size_t)255;
-  return acc_al + (size_t)b * h * s * sizeof(float);
+// Workspace: the fp32 dQ accumulator, then D and lse2 (each laid out per shard
+// with rows padded to a multiple of 128), each part 256-byte aligned.
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+long long stat_rows_per_shard(long long s, int n_shards) {
+  const long long L = s / n_shards;
+  return (L + kTileM - 1) / kTileM * kTileM;
+}
+size_t bwd_ws_bytes(long long b, long long h, long long s, long long d, int n_shards) {
+  const size_t acc = round256((size_t)b * h * s * d * sizeof(float));
+  const size_t stats = round256((size_t)b * h * n_shards * stat_rows_per_shard(s, n_shards) * sizeof(float));
+  return acc + 2 * stats;
 }
 
 ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
@@ -258,10 +265,13 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(check_scale(scale));
   if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
   if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, q.d)) return RA_ERR_WORKSPACE;
+  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, q.d, n_shards)) return RA_ERR_WORKSPACE;
   float* dq_acc = static_cast<float*>(ws);
-  const size_t acc = (size_t)q.b * q.h * q.s * q.d * sizeof(float);
-  float* Dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + ((acc + 255) & ~(size_t)255));
+  const int stat_L = (int)stat_rows_per_shard(q.s, n_shards);
+  const size_t acc = round256((size_t)q.b * q.h * q.s * q.d * sizeof(float));
+  const size_t stats = round256((size_t)q.b * q.h * n_shards * stat_L * sizeof(float));
+  float* Dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc + stats);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   View4 vdo{dout.data, dout.sb, dout.sh, dout.ss, (int)dout.b, (int)dout.h, (int)dout.s, (int)dout.d};
@@ -281,10 +291,8 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.n_ktiles = (p.L + kTileN - 1) / kTileN;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.lse = lse;
-  p.l_sb = lsb;
-  p.l_sh = lsh;
-  p.l_ss = lss;
+  p.stat_L = stat_L;
+  p.lse2 = lse2;
   p.Dsum = Dsum;
   p.dq_acc = dq_acc;
   p.dk = dk.data;
@@ -305,7 +313,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, Dsum, dq_acc, st)));
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, Dsum, lse2, dq_acc, n_shards, stat_L, st)));
   }
   {
     TimedLaunch tl(RA_KERNEL_BWD, st);
@@ -552,9 +560,9 @@ ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, 
   return permute_common(y, x, layout, n_shards, seq_dim, 1, stream);
 }
 
-size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d) {
-  if (b < 1 || h < 1 || s < 1 || d < 1) return 0;
-  if (op == RA_OP_BWD) return bwd_ws_bytes(b, h, s, d);
+size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards) {
+  if (b < 1 || h < 1 || s < 1 || d < 1 || n_shards < 1 || s % n_shards) return 0;
+  if (op == RA_OP_BWD) return bwd_ws_bytes(b, h, s, d, n_shards);
   return 0;
 }
 

@@ -34,9 +34,9 @@ struct BwdParams {
   int n_qtiles, n_ktiles;   // tiles per shard
   float scale;              // softmax scale
   float scale_log2;
-  const float* lse;         // (b, h, s) natural log, element strides
-  long long l_sb, l_sh, l_ss;
-  const float* Dsum;        // rowsum(dO * O), packed (b, h, s)
+  int stat_L;               // per-shard rows of the statistics arrays: n_qtiles * 128
+  const float* lse2;        // lse * log2(e), (b, h, shard, stat_L); padding rows hold +inf
+  const float* Dsum;        // rowsum(dO * O), same layout; padding rows hold 0
   float* dq_acc;            // fp32 (b, h, s, d) packed accumulator
   void* dk;                 // bf16 outputs
   void* dv;
@@ -62,8 +62,15 @@ cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
 size_t bwd_smem_bytes(int D);
 
-// D = rowsum(dO * O) (fp32, packed (b,h,s)) and zero of the dQ accumulator.
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, float* Dsum, float* dq_acc, cudaStream_t st);
+// Per query row: D = rowsum(dO * O) and lse2 = lse * log2(e), stored per shard
+// with the rows padded to stat_L (padding rows get D = 0, lse2 = +inf), and
+// the row of the fp32 dQ accumulator set to zero.
+struct LseView {
+  const float* data;
+  long long sb, sh, ss;
+};
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2,
+                           float* dq_acc, int N, int stat_L, cudaStream_t st);
 // dq (bf16) = dq_acc (fp32, packed).
 cudaError_t launch_bwd_post(const float* dq_acc, const View4& dq, cudaStream_t st);
 

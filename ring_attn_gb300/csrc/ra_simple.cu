@@ -110,23 +110,31 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
 }
 
 // ------------------------------------------------------------------ backward pre / post
-// D[b,h,p] = sum_d dO * O (fp32), and the fp32 dQ accumulator row set to zero.
-// 16 threads per row of d = 128 (8 bf16 each), 8 per row of d = 64.
-__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, float* Dsum, float* dq_acc) {
+// Per query row: D = sum_d dO * O and lse2 = lse * log2(e), stored per shard
+// with each shard's rows padded to stat_L (padding: D = 0, lse2 = +inf, so a
+// padded column contributes P = 0 and dS = 0), and the row of the fp32 dQ
+// accumulator set to zero.  d/8 threads per row (8 bf16 each).
+__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* Dsum,
+                                                            float* lse2, float* dq_acc, int N, int stat_L) {
   const int tpr = dout.d / 8;  // threads per row
-  const long long rows = (long long)dout.b * dout.h * dout.s;
+  const int L = dout.s / N;
+  const long long rows = (long long)dout.b * dout.h * N * stat_L;
   const long long total = rows * tpr;
   const long long step = (long long)gridDim.x * blockDim.x;
   // tpr divides 32, so each row's threads sit in one warp and stay converged
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t - threadIdx.x % 32 < total; t += step) {
     const bool live = t < total;
-    const long long row = live ? t / tpr : 0;
+    const long long row = live ? t / tpr : 0;  // (b, h, shard, padded local row)
     const int part = (int)(t % tpr);
-    const long long p = row % dout.s;
-    const long long bh = row / dout.s;
+    const int i = (int)(row % stat_L);
+    const long long bhr = row / stat_L;
+    const int r = (int)(bhr % N);
+    const long long bh = bhr / N;
     const long long h = bh % dout.h, b = bh / dout.h;
+    const bool real = live && i < L;
+    const long long p = (long long)r * L + i;  // layout position
     float acc = 0.f;
-    if (live) {
+    if (real) {
       const uint4 x = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dout.data) +
                                                            b * dout.sb + h * dout.sh + p * dout.ss) + part);
       const uint4 y = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(out.data) +
@@ -140,12 +148,15 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
         acc = fmaf(a.x, c.x, acc);
         acc = fmaf(a.y, c.y, acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + row * dout.d) + 2 * part;
+      float4* z = reinterpret_cast<float4*>(dq_acc + ((long long)bh * dout.s + p) * dout.d) + 2 * part;
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && part == 0) Dsum[row] = acc;
+    if (live && part == 0) {
+      Dsum[row] = acc;
+      lse2[row] = real ? lse.data[b * lse.sb + h * lse.sh + p * lse.ss] * 1.4426950408889634f : INFINITY;
+    }
   }
 }
 
@@ -214,9 +225,10 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, float* Dsum, float* dq_acc, cudaStream_t st) {
-  const long long total = (long long)dout.b * dout.h * dout.s * (dout.d / 8);
-  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, Dsum, dq_acc);
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2,
+                           float* dq_acc, int N, int stat_L, cudaStream_t st) {
+  const long long total = (long long)dout.b * dout.h * N * stat_L * (dout.d / 8);
+  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, Dsum, lse2, dq_acc, N, stat_L);
   return cudaGetLastError();
 }
 

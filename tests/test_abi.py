@@ -45,10 +45,15 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.ring_attn_workspace_size(0, 1, 2, 256, 64) == 0
+    assert lib.ring_attn_workspace_size(0, 1, 2, 256, 64, 2) == 0
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     acc = 1 * 2 * 256 * 64 * 4
-    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64) == ((acc + 255) // 256) * 256 + 1 * 2 * 256 * 4
-    assert lib.ring_attn_workspace_size(1, 0, 2, 256, 64) == 0
+    # 2 shards of 128 rows: no padding
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 2) == r256(acc) + 2 * r256(1 * 2 * 2 * 128 * 4)
+    # 4 shards of 64 rows: each padded to 128
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 4) == r256(acc) + 2 * r256(1 * 2 * 4 * 128 * 4)
+    assert lib.ring_attn_workspace_size(1, 0, 2, 256, 64, 2) == 0
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 3) == 0
 
 
 def _fake(shape, dtype=ra.RA_BF16, data=0x10000, strides=None):

@@ -59,7 +59,7 @@ def _run(ra, w):
         res["out"] = back(out)
         res["lse"] = back(lse)
         if w.backward:
-            ws = torch.empty(ra.ring_attn_workspace_size(1, w.b, w.h, w.s, w.d), dtype=torch.uint8, device=dev)
+            ws = torch.empty(ra.ring_attn_workspace_size(1, w.b, w.h, w.s, w.d, w.n_shards), dtype=torch.uint8, device=dev)
             dq, dk, dv = ra.ring_attn_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, w.layout, w.n_shards,
                                           w.causal, scale, workspace=ws)
             res["dq"], res["dk"], res["dv"] = back(dq), back(dk), back(dv)
