@@ -40,7 +40,7 @@ WORKLOAD = "causal zigzag fwd+bwd: b1 h32 s65536 d128, 8 shards (chunks r and 15
 FWD_FLOP = 4.0 * B * H * S * S * D / 2.0          # causal-adjusted forward
 STEP_FLOP = 2.5 * FWD_FLOP                         # fwd+bwd, 2.5x convention
 STEP_FLOP_ALG = 3.5 * FWD_FLOP                     # fwd + bwd (5 GEMMs vs 2)
-BWD_FLOP = 2.5 * FWD_FLOP                          # backward kernel alone: 10*d per unmasked pair
+BWD_FLOP = 2.5 * FWD_FLOP                          # backward alone: 10*d per unmasked pair
 CPU_SAMPLE_TOKENS = 8192       # reference arm: one step of CPU work
 CPU_BASELINE_TOKENS = 16384    # cpu_baseline: ~10-30 s of CPU work
 
@@ -306,21 +306,32 @@ def main():
         raise RuntimeError(f"device error {st} info {info:#x} in the timed region")
     ms = max_over_ranks(ms, dist, dev)
 
-    fwd_ms = kt["fwd"][0] / max(kt["fwd"][1], 1)
-    bwd_ms = kt["bwd"][0] / max(kt["bwd"][1], 1)
+    def avg(name):
+        return kt[name][0] / max(kt[name][1], 1)
+
+    fwd_ms, dkdv_ms, dq_ms, pre_ms = avg("fwd"), avg("bwd_dkdv"), avg("bwd_dq"), avg("bwd_pre")
+    bwd_ms = dkdv_ms + dq_ms + pre_ms
     value = job_tflops(world, STEP_FLOP, ms)
     bwd_tflops = BWD_FLOP / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = FWD_FLOP / (fwd_ms * 1e-3) / 1e12
     peak_sus = peaks["bf16_sustained"]
-    bwd_src = ["ring_attn_gb300/csrc/ra_bwd.cu", "ring_attn_gb300/csrc/ra_device.cuh",
-               "ring_attn_gb300/csrc/ra_internal.h"]
-    fwd_src = ["ring_attn_gb300/csrc/ra_fwd.cu", "ring_attn_gb300/csrc/ra_device.cuh",
-               "ring_attn_gb300/csrc/ra_internal.h"]
-    roofline = {"kernel": "ring_bwd_kernel<128>", "bound": "tensor", "achieved": bwd_tflops, "peak": peak_sus,
-                "unit": "TFLOP/s", "frac": bwd_tflops / peak_sus,
-                "traffic": _profiled_traffic("ring_bwd_kernel_zigzag_h32_s64k.md", bwd_src),
-                "algorithmic_flop_per_launch": BWD_FLOP,
-                "peak_kind": f"bf16 sustained ({peaks['source']})", "launch_ms": bwd_ms}
+    # FLOP each kernel performs: forward 2 GEMMs, dK/dV 4 GEMMs, dQ 3 GEMMs (S and dP recomputed)
+    kernels = {
+        "ring_fwd_kernel<128>": (fwd_ms, FWD_FLOP, ["ring_attn_gb300/csrc/ra_fwd.cu"], "ring_fwd_kernel_zigzag_h32_s64k.md"),
+        "ring_dkdv_kernel<128>": (dkdv_ms, 2.0 * FWD_FLOP, ["ring_attn_gb300/csrc/ra_bwd.cu"],
+                                  "ring_dkdv_kernel_zigzag_h32_s64k.md"),
+        "ring_dq_kernel<128>": (dq_ms, 1.5 * FWD_FLOP, ["ring_attn_gb300/csrc/ra_bwd.cu"],
+                                "ring_dq_kernel_zigzag_h32_s64k.md"),
+    }
+    common = ["ring_attn_gb300/csrc/ra_device.cuh", "ring_attn_gb300/csrc/ra_internal.h",
+              "ring_attn_gb300/csrc/ra_tiles.cuh"]
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    d_ms, d_flop, d_src, d_prof = kernels[dom]
+    d_tflops = d_flop / (d_ms * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": d_tflops, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": d_tflops / peak_sus, "traffic": _profiled_traffic(d_prof, d_src + common),
+                "algorithmic_flop_per_launch": d_flop, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                "launch_ms": d_ms}
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -330,10 +341,12 @@ def main():
                    "l2": "no flush: inputs larger than L2 (q, k, v, dO 512 MiB each)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd": {"tflops": fwd_tflops, "ms": fwd_ms, "frac_of_peak": fwd_tflops / peak_sus,
-                "traffic": _profiled_traffic("ring_fwd_kernel_zigzag_h32_s64k.md", fwd_src)},
+                "traffic": _profiled_traffic("ring_fwd_kernel_zigzag_h32_s64k.md",
+                                             ["ring_attn_gb300/csrc/ra_fwd.cu"] + common)},
         "bwd": {"tflops": bwd_tflops, "ms": bwd_ms, "frac_of_peak": bwd_tflops / peak_sus,
-                "pre_ms": kt["bwd_pre"][0] / max(kt["bwd_pre"][1], 1),
-                "post_ms": kt["bwd_post"][0] / max(kt["bwd_post"][1], 1)},
+                "flop_credited": "2.5 x forward (the 5 backward GEMMs; the 2 recomputed in the dQ pass are not)",
+                "dkdv_ms": dkdv_ms, "dkdv_tflops_performed": 2.0 * FWD_FLOP / (dkdv_ms * 1e-3) / 1e12,
+                "dq_ms": dq_ms, "dq_tflops_performed": 1.5 * FWD_FLOP / (dq_ms * 1e-3) / 1e12, "pre_ms": pre_ms},
         "fwd_bwd_frac_of_peak": value / world / peak_sus,
         "fwd_bwd_tflops_3p5x": job_tflops(world, STEP_FLOP_ALG, ms),
         "roofline": roofline, "gpu_launches": launches, "clocks": clk,

@@ -123,10 +123,12 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
  *   dq, dk, dv: (b, h, s, d) bf16 outputs, layout order.
  *   With P = exp(S - lse) recomputed from the saved lse:
  *   D = rowsum(dO * O), dV = P^T dO, dS = P * (dO V^T - D), dQ = scale dS K,
- *   dK = scale dS^T Q.  dK and dV stay tile-local in tensor memory; dQ is
- *   accumulated in fp32 in the workspace and cast at the end.
- *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards) bytes,
- *   256-byte aligned, owned by the caller, contents need not be initialised. */
+ *   dK = scale dS^T Q.  One kernel per key tile keeps dK and dV in tensor
+ *   memory while it meets the query tiles in ring order; one kernel per query
+ *   tile recomputes S and dP and keeps dQ in tensor memory.  No atomics: the
+ *   results are deterministic.
+ *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards)
+ *   bytes, 256-byte aligned, owned by the caller, need not be initialised. */
 ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                         const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
                         int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
@@ -165,10 +167,10 @@ ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, 
                               void* stream);
 
 /* Workspace bytes needed by `op` (ra_op) for (b, h, s, d) split into n_shards
- * shards; 0 for RA_OP_FWD.  RA_OP_BWD: an fp32 dQ accumulator (b*h*s*d), then
- * D = rowsum(dO*O) and lse*log2(e) per query row, each laid out per shard with
- * the shard's rows padded to a multiple of 128 (b*h*n_shards*ceil(s/n_shards/128)*128
- * floats each); every part 256-byte aligned.  Varlen calls use b = 1, s = total. */
+ * shards; 0 for RA_OP_FWD.  RA_OP_BWD: D = rowsum(dO*O) and lse*log2(e) per
+ * query row, each laid out per shard with the shard's rows padded to a
+ * multiple of 128 (b*h*n_shards*ceil(s/n_shards/128)*128 floats each), each
+ * part 256-byte aligned.  Varlen calls use b = 1, s = total.  0 on bad sizes. */
 size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards);
 
 /* Synchronises `stream`, then reads and clears this device's error word.
@@ -192,9 +194,9 @@ ra_status ring_attn_set_knob(int32_t knob, int64_t value);
  * them.  Disabling drops anything not yet read. */
 typedef enum {
   RA_KERNEL_FWD = 0,       /* ring forward (fused merge, or one ring step) */
-  RA_KERNEL_BWD = 1,       /* ring backward main kernel */
-  RA_KERNEL_BWD_PRE = 2,   /* D = rowsum(dO * O), dQ accumulator cleared */
-  RA_KERNEL_BWD_POST = 3,  /* dQ fp32 -> bf16 */
+  RA_KERNEL_BWD = 1,       /* ring backward: the dK / dV kernel */
+  RA_KERNEL_BWD_PRE = 2,   /* D = rowsum(dO * O) and lse * log2(e) per query row */
+  RA_KERNEL_BWD_DQ = 3,    /* ring backward: the dQ kernel */
   RA_KERNEL_PERMUTE = 4,   /* permute / unpermute */
   RA_KERNEL_LSE_MERGE = 5,
   RA_KERNEL_COUNT = 6

@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
     "ra_status_string", "ring_attn_version",
 )
-KERNELS = {"fwd": 0, "bwd": 1, "bwd_pre": 2, "bwd_post": 3, "permute": 4, "lse_merge": 5}
+KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
 
 
 class RingAttnError(RuntimeError):

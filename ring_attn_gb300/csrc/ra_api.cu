@@ -240,17 +240,15 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   return cuda_status(launch_fwd((int)q.d, tq, tk, tv, p, static_cast<cudaStream_t>(stream)));
 }
 
-// Workspace: the fp32 dQ accumulator, then D and lse2 (each laid out per shard
-// with rows padded to a multiple of 128), each part 256-byte aligned.
+// Workspace: D and lse2, each laid out per shard with rows padded to a
+// multiple of 128, each part 256-byte aligned.
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 long long stat_rows_per_shard(long long s, int n_shards) {
   const long long L = s / n_shards;
   return (L + kTileM - 1) / kTileM * kTileM;
 }
-size_t bwd_ws_bytes(long long b, long long h, long long s, long long d, int n_shards) {
-  const size_t acc = round256((size_t)b * h * s * d * sizeof(float));
-  const size_t stats = round256((size_t)b * h * n_shards * stat_rows_per_shard(s, n_shards) * sizeof(float));
-  return acc + 2 * stats;
+size_t bwd_ws_bytes(long long b, long long h, long long s, int n_shards) {
+  return 2 * round256((size_t)b * h * n_shards * stat_rows_per_shard(s, n_shards) * sizeof(float));
 }
 
 ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
@@ -265,18 +263,15 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(check_scale(scale));
   if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
   if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, q.d, n_shards)) return RA_ERR_WORKSPACE;
-  float* dq_acc = static_cast<float*>(ws);
+  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, n_shards)) return RA_ERR_WORKSPACE;
   const int stat_L = (int)stat_rows_per_shard(q.s, n_shards);
-  const size_t acc = round256((size_t)q.b * q.h * q.s * q.d * sizeof(float));
   const size_t stats = round256((size_t)q.b * q.h * n_shards * stat_L * sizeof(float));
-  float* Dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc);
-  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc + stats);
+  float* Dsum = static_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + stats);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   View4 vdo{dout.data, dout.sb, dout.sh, dout.ss, (int)dout.b, (int)dout.h, (int)dout.s, (int)dout.d};
   View4 vo{out.data, out.sb, out.sh, out.ss, (int)out.b, (int)out.h, (int)out.s, (int)out.d};
-  View4 vdq{dq.data, dq.sb, dq.sh, dq.ss, (int)dq.b, (int)dq.h, (int)dq.s, (int)dq.d};
 
   BwdParams p;
   memset(&p, 0, sizeof(p));
@@ -294,9 +289,12 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.stat_L = stat_L;
   p.lse2 = lse2;
   p.Dsum = Dsum;
-  p.dq_acc = dq_acc;
+  p.dq = dq.data;
   p.dk = dk.data;
   p.dv = dv.data;
+  p.q_sb = dq.sb;
+  p.q_sh = dq.sh;
+  p.q_ss = dq.ss;
   p.k_sb = dk.sb;
   p.k_sh = dk.sh;
   p.k_ss = dk.ss;
@@ -313,14 +311,14 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, Dsum, lse2, dq_acc, n_shards, stat_L, st)));
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, Dsum, lse2, n_shards, stat_L, st)));
   }
   {
     TimedLaunch tl(RA_KERNEL_BWD, st);
-    RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, st)));
+    RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 0, st)));
   }
-  TimedLaunch tl(RA_KERNEL_BWD_POST, st);
-  return cuda_status(launch_bwd_post(dq_acc, vdq, st));
+  TimedLaunch tl(RA_KERNEL_BWD_DQ, st);
+  return cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 1, st));
 }
 
 ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs, int32_t max_seqlen,
@@ -436,6 +434,33 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
   a.lb_s0 = lb[0];
   a.lb_s1 = lb[1];
   a.lb_s2 = lb[2];
+  // rows that collapse to one stride per tensor are indexed without divisions:
+  // walk the non-unit row dims from the inside out, each must step by the
+  // previous dim's extent; the innermost non-unit stride is the row stride
+  auto row_stride = [&](const long long* st, long long* out) {
+    long long stride = 0, expect = -1;
+    for (int i = 2; i >= 0; --i) {
+      if (n[i] == 1) continue;
+      if (expect < 0) {
+        stride = st[i];
+      } else if (st[i] != expect) {
+        return false;
+      }
+      expect = st[i] * n[i];
+    }
+    *out = stride;
+    return true;
+  };
+  long long f_oa, f_ob, f_la, f_lb;
+  a.flat = row_stride(oa, &f_oa) && row_stride(ob, &f_ob) && row_stride(la, &f_la) && row_stride(lb, &f_lb);
+  if (a.flat) {  // the kernel then reads only the *_s2 strides
+    a.oa_s2 = f_oa;
+    a.ob_s2 = f_ob;
+    a.la_s2 = f_la;
+    a.lb_s2 = f_lb;
+  }
+  a.qshift = 0;
+  while ((1LL << a.qshift) < d / 4) ++a.qshift;
   TimedLaunch tl(RA_KERNEL_LSE_MERGE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_lse_merge(a, static_cast<cudaStream_t>(stream)));
 }
@@ -562,7 +587,7 @@ ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, 
 
 size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards) {
   if (b < 1 || h < 1 || s < 1 || d < 1 || n_shards < 1 || s % n_shards) return 0;
-  if (op == RA_OP_BWD) return bwd_ws_bytes(b, h, s, d, n_shards);
+  if (op == RA_OP_BWD) return bwd_ws_bytes(b, h, s, n_shards);
   return 0;
 }
 

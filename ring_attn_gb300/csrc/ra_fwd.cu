@@ -35,7 +35,7 @@
 // earlier MMA of the issuing thread), so a softmax thread may rescale O_t as
 // soon as its S tile is ready.  Empty key tiles are never loaded; only
 // partial tiles are masked element by element.
-#include "ra_internal.h"
+#include "ra_tiles.cuh"
 
 namespace ra {
 namespace {
@@ -82,85 +82,12 @@ enum FwdBar {
   B_TEARDOWN = 16
 };
 
-// Rows [i0, i0 + rows) of Q shard r; the valid ones end at i_last.
-struct QRange {
-  int r, i0, i_last;
-  int gq_lo, gq_hi;    // original token indices of the first / last valid row
-  int key_lo, key_hi;  // varlen: keys any row may see (inclusive)
-  int seg_single;            // varlen: the segment of every valid row, or -1
-};
-
-__device__ __forceinline__ void make_range(const FwdParams& p, int r, int i0, int rows, QRange& q) {
-  q.r = r;
-  q.i0 = i0;
-  q.i_last = min(i0 + rows, p.L) - 1;
-  const int ilo = min(i0, p.L - 1);
-  q.gq_lo = token_of(p.layout, p.N, p.L, r, ilo);
-  q.gq_hi = token_of(p.layout, p.N, p.L, r, max(q.i_last, ilo));
-  q.key_lo = q.key_hi = 0;
-  q.seg_single = -1;
-  if (p.cu) {
-    const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
-    const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
-    q.key_lo = __ldg(p.cu + sa);
-    q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
-    q.seg_single = sa == sz ? sa : -1;
-  }
-}
-
-// Key-tile range [lo, hi) of KV shard s that can hold a key allowed for some row of q.
-__device__ __forceinline__ void kv_range(const FwdParams& p, const QRange& q, int s, int nkt, int& lo, int& hi) {
-  if (p.cu) {
-    const int base = s * p.L;
-    int jlo = q.key_lo - base, jhi = q.key_hi - base;
-    if (jlo < 0) jlo = 0;
-    if (jhi > p.L - 1) jhi = p.L - 1;
-    if (jlo > jhi) {
-      lo = hi = 0;
-      return;
-    }
-    lo = jlo / kTileN;
-    hi = jhi / kTileN + 1;
-    return;
-  }
-  lo = 0;
-  if (!p.causal) {
-    hi = nkt;
-    return;
-  }
-  // token_of is increasing inside a shard, so the allowed keys of the largest
-  // row token are a prefix of the shard and cover every other row's keys.
-  const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, q.gq_hi);
-  hi = jm < 0 ? 0 : jm / kTileN + 1;
-}
-
-// True when every (valid row of q, key) pair of the tile is allowed: no masking needed.
-__device__ __forceinline__ bool tile_full(const FwdParams& p, const QRange& q, int s, int kt) {
-  const int j0 = kt * kTileN;
-  if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
-  if (p.cu) {
-    if (q.seg_single < 0) return false;
-    const int base = s * p.L + j0;
-    const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
-    if (base < slo || base + kTileN > shi) return false;
-    return !p.causal || q.gq_lo >= base + kTileN - 1;
-  }
-  return !p.causal || q.gq_lo >= token_of(p.layout, p.N, p.L, s, j0 + kTileN - 1);
-}
-
-// Calls f(s, kt) for every key tile the CTA's rows meet, in ring order.
+// The CTA's key tiles, in ring order (all ring steps, or the one the step mode asks for).
 template <class F>
 __device__ __forceinline__ void walk_tiles(const FwdParams& p, const QRange& q, int nkt, F&& f) {
   const int t0 = p.step < 0 ? 0 : p.step;
   const int t1 = p.step < 0 ? p.N : p.step + 1;
-  for (int t = t0; t < t1; ++t) {
-    int s = q.r - t;
-    if (s < 0) s += p.N;
-    int lo, hi;
-    kv_range(p, q, s, nkt, lo, hi);
-    for (int kt = lo; kt < hi; ++kt)
-      if (!f(s, kt)) return;
-  }
+  walk_kv_tiles(p, q, nkt, t0, t1, f);
 }
 
 template <int D>
@@ -183,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = x / n_pairs;
   const int i0 = (x % n_pairs) * kRowsPerCta;
   QRange cta;  // both query tiles together: decides which key tiles are visited
-  make_range(p, r, i0, kRowsPerCta, cta);
+  make_qrange(p, r, i0, kRowsPerCta, cta);
   const int nkt = (p.L + kTileN - 1) / kTileN;
   int n_tiles = 0;
   walk_tiles(p, cta, nkt, [&](int, int) {
@@ -344,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tl + LY::kTmemS + t * 128;
     const uint32_t tO = tl + LY::kTmemO + t * 128;
     QRange qt;
-    make_range(p, r, i0 + t * kTileM, kTileM, qt);
+    make_qrange(p, r, i0 + t * kTileM, kTileM, qt);
     const int i = i0 + t * kTileM + row;
     const bool valid = i < p.L;
     const int gq = token_of(p.layout, p.N, p.L, r, valid ? i : max(qt.i_last, 0));
@@ -366,20 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // column window [c_lo, c_hi) of allowed keys for this row (all 128 when the tile is full)
       int c_lo = 0, c_hi = kTileN;
-      if (!tile_full(p, qt, s, kt)) {
-        const int j0 = kt * kTileN;
-        const int jlim = min(kTileN, p.L - j0);
-        c_hi = jlim;
-        if (p.cu) {
-          const int base = s * p.L + j0;
-          const int lo = rk_lo - base, hi = rk_hi - base;
-          c_lo = lo < 0 ? 0 : (lo > kTileN ? kTileN : lo);
-          c_hi = hi < 0 ? 0 : (hi > jlim ? jlim : hi);
-        } else if (p.causal) {
-          const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, gq);
-          c_hi = min(jlim, jm - j0 + 1);
-        }
-      }
+      if (!kv_tile_full(p, qt, s, kt)) row_key_window(p, gq, rk_lo, rk_hi, s, kt, c_lo, c_hi);
       const bool masked = c_lo > 0 || c_hi < kTileN;
       // all 128 scores of the row in registers: four loads, one wait
       uint32_t v[kTileN];

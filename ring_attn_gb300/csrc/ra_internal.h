@@ -32,14 +32,15 @@ struct BwdParams {
   int B, H, N, L, S;
   int layout, causal;
   int n_qtiles, n_ktiles;   // tiles per shard
+  int stat_L;               // per-shard rows of the statistics arrays: n_qtiles * 128
   float scale;              // softmax scale
   float scale_log2;
-  int stat_L;               // per-shard rows of the statistics arrays: n_qtiles * 128
   const float* lse2;        // lse * log2(e), (b, h, shard, stat_L); padding rows hold +inf
   const float* Dsum;        // rowsum(dO * O), same layout; padding rows hold 0
-  float* dq_acc;            // fp32 (b, h, s, d) packed accumulator
-  void* dk;                 // bf16 outputs
+  void* dq;                 // bf16 outputs
+  void* dk;
   void* dv;
+  long long q_sb, q_sh, q_ss;   // strides of dq
   long long k_sb, k_sh, k_ss;   // strides of dk
   long long v_sb, v_sh, v_ss;   // strides of dv
   const int* cu;
@@ -58,21 +59,18 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdParams& p, cudaStream_t st);
 size_t fwd_smem_bytes(int D);
 
+// which = 0: the dK / dV kernel; 1: the dQ kernel.
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
-size_t bwd_smem_bytes(int D);
+                       const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st);
 
 // Per query row: D = rowsum(dO * O) and lse2 = lse * log2(e), stored per shard
-// with the rows padded to stat_L (padding rows get D = 0, lse2 = +inf), and
-// the row of the fp32 dQ accumulator set to zero.
+// with the rows padded to stat_L (padding rows get D = 0, lse2 = +inf).
 struct LseView {
   const float* data;
   long long sb, sh, ss;
 };
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2,
-                           float* dq_acc, int N, int stat_L, cudaStream_t st);
-// dq (bf16) = dq_acc (fp32, packed).
-cudaError_t launch_bwd_post(const float* dq_acc, const View4& dq, cudaStream_t st);
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2, int N,
+                           int stat_L, cudaStream_t st);
 
 struct MergeArgs {
   float* out_acc;        // rows x d, row stride (elements)
@@ -87,6 +85,8 @@ struct MergeArgs {
   long long la_s0, la_s1, la_s2;
   long long ob_s0, ob_s1, ob_s2;
   long long lb_s0, lb_s1, lb_s2;
+  int flat;              // the three row dims collapse to one stride per tensor (the *_s2 strides)
+  int qshift;            // log2(d / 4)
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st);
 
@@ -101,6 +101,7 @@ struct PermuteArgs {
   long long src_seq_stride, dst_seq_stride;
   int s, layout, N;
   int inverse;              // 0: dst[p] = src[g(p)]; 1: dst[g(p)] = src[p]
+  int vpr_total;            // vectors per row (set by the launcher)
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 

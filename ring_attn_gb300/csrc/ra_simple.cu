@@ -1,6 +1,5 @@
 // Memory-bound kernels of the ring-attention path: shard-layout permutation,
-// the standalone LSE merge, the backward preprocess D = rowsum(dO * O) and
-// the final cast of the fp32 dQ accumulator.  All are grid-stride loops with
+// the standalone LSE merge and the backward preprocess D = rowsum(dO * O).  All are grid-stride loops with
 // 16-byte accesses, sized to a multiple of the SM count.
 #include "ra_internal.h"
 
@@ -18,22 +17,24 @@ int grid_for(long long work_items, int per_block) {
 }
 
 // ------------------------------------------------------------------ permutation
-// A "row" is the packed run of elements after the sequence dimension.  Each
-// thread moves 16 bytes when the row allows it, else one element.
+// A "row" is the packed run of elements after the sequence dimension, moved as
+// vpr vectors V (16 bytes when the row allows it).  A block handles
+// rows_per_block rows per turn, vpr threads per row, so the row's source and
+// destination are decoded once per thread and turn, not per element.
 template <typename V>
-__global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, long long vec_per_row) {
-  const long long total = a.n_outer * a.s * vec_per_row;
-  const long long step = (long long)gridDim.x * blockDim.x;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += step) {
-    const long long v = t % vec_per_row;
-    const long long rp = t / vec_per_row;
+__global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vpr, int rows_per_block) {
+  const long long total_rows = a.n_outer * a.s;
+  const int rloc = threadIdx.x / vpr, v = threadIdx.x % vpr;
+  if (rloc >= rows_per_block) return;
+  const int L = a.s / a.N;
+  for (long long rp = (long long)blockIdx.x * rows_per_block + rloc; rp < total_rows;
+       rp += (long long)gridDim.x * rows_per_block) {
     const int p = (int)(rp % a.s);           // layout position
     long long o = rp / a.s;                  // outer index
     const long long o2 = o % a.outer_shape[2];
     o /= a.outer_shape[2];
     const long long o1 = o % a.outer_shape[1];
     const long long o0 = o / a.outer_shape[1];
-    const int L = a.s / a.N;
     const long long g = token_of(a.layout, a.N, L, p / L, p % L);  // original token at position p
     const long long src_pos = a.inverse ? p : g;
     const long long dst_pos = a.inverse ? g : p;
@@ -41,9 +42,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, long l
                          src_pos * a.src_seq_stride;
     const long long dof = o0 * a.dst_outer_stride[0] + o1 * a.dst_outer_stride[1] + o2 * a.dst_outer_stride[2] +
                           dst_pos * a.dst_seq_stride;
-    const char* s = reinterpret_cast<const char*>(a.src) + so * a.esize;
-    char* d = reinterpret_cast<char*>(a.dst) + dof * a.esize;
-    reinterpret_cast<V*>(d)[v] = reinterpret_cast<const V*>(s)[v];
+    const V* src = reinterpret_cast<const V*>(reinterpret_cast<const char*>(a.src) + so * a.esize);
+    V* dst = reinterpret_cast<V*>(reinterpret_cast<char*>(a.dst) + dof * a.esize);
+    for (int k = v; k < a.vpr_total; k += vpr) dst[k] = __ldg(src + k);
   }
 }
 
@@ -52,70 +53,90 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, long l
 // owns a row, 4 columns per thread:
 //   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
 //   out_acc += w * (out_blk - out_acc).
-// Loop control is warp-uniform so that every lane of the row has read the old
-// lse_acc (before __syncwarp) before the row's first lane overwrites it.
+// Each thread handles kUnroll rows per loop turn and issues every load before
+// using any, so that enough bytes are in flight to keep HBM busy.  Loop
+// control is warp-uniform: every lane of a row has read the old lse_acc
+// (before __syncwarp) before the row's first lane overwrites it.
+constexpr int kUnroll = 2;
+
 template <bool BLK_F32>
 __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
   const long long q_per_row = a.d / 4;
   const long long total = a.rows * q_per_row;
   const long long step = (long long)gridDim.x * blockDim.x;
   const int lane = threadIdx.x & 31;
-  for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x - lane; base < total; base += step) {
-    const long long t = base + lane;
-    const bool live = t < total;
-    const long long c4 = live ? t % q_per_row : 0;
-    long long rw = live ? t / q_per_row : 0;
-    const long long i2 = rw % a.n2;
-    rw /= a.n2;
-    const long long i1 = rw % a.n1;
-    const long long i0 = rw / a.n1;
-    float* oa = a.out_acc + i0 * a.oa_s0 + i1 * a.oa_s1 + i2 * a.oa_s2 + 4 * c4;
-    float* la = a.lse_acc + i0 * a.la_s0 + i1 * a.la_s1 + i2 * a.la_s2;
-    const float* lb = a.lse_blk + i0 * a.lb_s0 + i1 * a.lb_s1 + i2 * a.lb_s2;
-    const long long bofs = i0 * a.ob_s0 + i1 * a.ob_s1 + i2 * a.ob_s2 + 4 * c4;
-    const float A = live ? *la : 0.f;
-    const float B = live ? __ldg(lb) : -INFINITY;
+  for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x - lane; base < total;
+       base += kUnroll * step) {
+    float* oa[kUnroll];
+    float* la[kUnroll];
+    float A[kUnroll], B[kUnroll];
+    float4 ob[kUnroll], oc[kUnroll];
+    bool live[kUnroll];
+    long long c4[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long t = base + u * step + lane;
+      live[u] = t < total;
+      c4[u] = live[u] ? (t & (q_per_row - 1)) : 0;  // d / 4 is a power of two
+      long long rw = live[u] ? (t >> a.qshift) : 0;
+      long long i0 = 0, i1 = 0, i2 = rw;
+      if (!a.flat) {
+        i2 = rw % a.n2;
+        rw /= a.n2;
+        i1 = rw % a.n1;
+        i0 = rw / a.n1;
+      }
+      oa[u] = a.out_acc + i0 * a.oa_s0 + i1 * a.oa_s1 + i2 * a.oa_s2 + 4 * c4[u];
+      la[u] = a.lse_acc + i0 * a.la_s0 + i1 * a.la_s1 + i2 * a.la_s2;
+      const float* lb = a.lse_blk + i0 * a.lb_s0 + i1 * a.lb_s1 + i2 * a.lb_s2;
+      const long long bofs = i0 * a.ob_s0 + i1 * a.ob_s1 + i2 * a.ob_s2 + 4 * c4[u];
+      A[u] = live[u] ? *la[u] : 0.f;
+      B[u] = live[u] ? __ldg(lb) : -INFINITY;
+      oc[u] = live[u] ? *reinterpret_cast<const float4*>(oa[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (BLK_F32) {
+        ob[u] = live[u] ? __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const uint2 raw = live[u] ? __ldg(reinterpret_cast<const uint2*>(
+                                        reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs))
+                                  : make_uint2(0u, 0u);
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        ob[u] = make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+      }
+    }
     __syncwarp();
-    if (!live) continue;
-    if (B == -INFINITY) {
-      // empty block: the accumulator is unchanged, except that an empty
-      // accumulator (lse -inf) is normalised to out = 0
-      if (A == -INFINITY) *reinterpret_cast<float4*>(oa) = make_float4(0.f, 0.f, 0.f, 0.f);
-      continue;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (!live[u]) continue;
+      float4 r;
+      float lse_new;
+      if (B[u] == -INFINITY) {
+        // empty block: unchanged, except that an empty accumulator is normalised to out = 0
+        if (A[u] != -INFINITY) continue;
+        r = make_float4(0.f, 0.f, 0.f, 0.f);
+        lse_new = -INFINITY;
+      } else if (A[u] == -INFINITY) {
+        r = ob[u];  // empty accumulator: take the block
+        lse_new = B[u];
+      } else {
+        lse_new = fmaxf(A[u], B[u]) + log1pf(expf(-fabsf(A[u] - B[u])));
+        const float w = expf(B[u] - lse_new);
+        r = make_float4(oc[u].x + w * (ob[u].x - oc[u].x), oc[u].y + w * (ob[u].y - oc[u].y),
+                        oc[u].z + w * (ob[u].z - oc[u].z), oc[u].w + w * (ob[u].w - oc[u].w));
+      }
+      *reinterpret_cast<float4*>(oa[u]) = r;
+      if (c4[u] == 0) *la[u] = lse_new;
     }
-    float4 ob;
-    if (BLK_F32) {
-      ob = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs));
-    } else {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs));
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      ob = make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
-    }
-    float4 r;
-    float lse_new;
-    if (A == -INFINITY) {
-      r = ob;  // empty accumulator: take the block
-      lse_new = B;
-    } else {
-      const float4 oacc = *reinterpret_cast<const float4*>(oa);
-      lse_new = fmaxf(A, B) + log1pf(expf(-fabsf(A - B)));
-      const float w = expf(B - lse_new);
-      r = make_float4(oacc.x + w * (ob.x - oacc.x), oacc.y + w * (ob.y - oacc.y), oacc.z + w * (ob.z - oacc.z),
-                      oacc.w + w * (ob.w - oacc.w));
-    }
-    *reinterpret_cast<float4*>(oa) = r;
-    if (c4 == 0) *la = lse_new;
   }
 }
 
 // ------------------------------------------------------------------ backward pre / post
 // Per query row: D = sum_d dO * O and lse2 = lse * log2(e), stored per shard
 // with each shard's rows padded to stat_L (padding: D = 0, lse2 = +inf, so a
-// padded column contributes P = 0 and dS = 0), and the row of the fp32 dQ
-// accumulator set to zero.  d/8 threads per row (8 bf16 each).
+// padded column contributes P = 0 and dS = 0).  d/8 threads per row (8 bf16 each).
 __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* Dsum,
-                                                            float* lse2, float* dq_acc, int N, int stat_L) {
+                                                            float* lse2, int N, int stat_L) {
   const int tpr = dout.d / 8;  // threads per row
   const int L = dout.s / N;
   const long long rows = (long long)dout.b * dout.h * N * stat_L;
@@ -148,37 +169,12 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
         acc = fmaf(a.x, c.x, acc);
         acc = fmaf(a.y, c.y, acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + ((long long)bh * dout.s + p) * dout.d) + 2 * part;
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && part == 0) {
       Dsum[row] = acc;
       lse2[row] = real ? lse.data[b * lse.sb + h * lse.sh + p * lse.ss] * 1.4426950408889634f : INFINITY;
     }
-  }
-}
-
-__global__ void __launch_bounds__(kThreads) bwd_post_kernel(const float* dq_acc, View4 dq) {
-  const int tpr = dq.d / 8;
-  const long long rows = (long long)dq.b * dq.h * dq.s;
-  const long long total = rows * tpr;
-  const long long step = (long long)gridDim.x * blockDim.x;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += step) {
-    const long long row = t / tpr;
-    const int part = (int)(t % tpr);
-    const long long p = row % dq.s;
-    const long long bh = row / dq.s;
-    const long long h = bh % dq.h, b = bh / dq.h;
-    const float4* src = reinterpret_cast<const float4*>(dq_acc + row * dq.d) + 2 * part;
-    const float4 u = __ldg(src), v = __ldg(src + 1);
-    uint4 o;
-    o.x = pack_bf16x2(u.x, u.y);
-    o.y = pack_bf16x2(u.z, u.w);
-    o.z = pack_bf16x2(v.x, v.y);
-    o.w = pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dq.data) + b * dq.sb + h * dq.sh + p * dq.ss)[part] = o;
   }
 }
 
@@ -196,7 +192,8 @@ int num_sms() {
   return cached[dev];
 }
 
-cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
+cudaError_t launch_permute(const PermuteArgs& a_in, cudaStream_t st) {
+  PermuteArgs a = a_in;
   const long long row_bytes = a.inner * a.esize;
   const bool vec16 = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(a.src) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.dst) % 16 == 0) && (a.src_seq_stride * a.esize) % 16 == 0 &&
@@ -205,14 +202,18 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
                      (a.dst_outer_stride[0] * a.esize) % 16 == 0 && (a.dst_outer_stride[1] * a.esize) % 16 == 0 &&
                      (a.dst_outer_stride[2] * a.esize) % 16 == 0;
   const long long total_rows = a.n_outer * a.s;
-  if (vec16) {
-    const long long vpr = row_bytes / 16;
-    permute_kernel<uint4><<<grid_for(total_rows * vpr, kThreads), kThreads, 0, st>>>(a, vpr);
-  } else if (a.esize == 4) {
-    permute_kernel<uint32_t><<<grid_for(total_rows * a.inner, kThreads), kThreads, 0, st>>>(a, a.inner);
-  } else {
-    permute_kernel<uint16_t><<<grid_for(total_rows * a.inner, kThreads), kThreads, 0, st>>>(a, a.inner);
-  }
+  const long long vpr_total = vec16 ? row_bytes / 16 : a.inner;
+  if (vpr_total > (1LL << 30)) return cudaErrorInvalidValue;
+  a.vpr_total = (int)vpr_total;
+  const int vpr = (int)(vpr_total < kThreads ? vpr_total : kThreads);  // threads per row
+  const int rows_per_block = kThreads / vpr;
+  const int grid = grid_for(total_rows, rows_per_block);
+  if (vec16)
+    permute_kernel<uint4><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
+  else if (a.esize == 4)
+    permute_kernel<uint32_t><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
+  else
+    permute_kernel<uint16_t><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
   return cudaGetLastError();
 }
 
@@ -225,17 +226,12 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2,
-                           float* dq_acc, int N, int stat_L, cudaStream_t st) {
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2, int N,
+                           int stat_L, cudaStream_t st) {
   const long long total = (long long)dout.b * dout.h * N * stat_L * (dout.d / 8);
-  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, Dsum, lse2, dq_acc, N, stat_L);
+  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, Dsum, lse2, N, stat_L);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, const View4& dq, cudaStream_t st) {
-  const long long total = (long long)dq.b * dq.h * dq.s * (dq.d / 8);
-  bwd_post_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dq_acc, dq);
-  return cudaGetLastError();
-}
 
 }  // namespace ra

@@ -1,0 +1,221 @@
+// Tile walks over the (Q shard, KV shard) pairs of the ring, shared by the
+// forward, the dQ pass and the dK/dV pass.
+//
+// The ring order is the pages' (guijiagi.com "Ring Attention：突破百万 Token
+// 上下文的分布式注意力", "详细流程"): at step t, Q shard r meets KV shard
+// (r - t) mod N, and KV shard s meets Q shard (s + t) mod N.  token_of is
+// increasing inside every shard for all three layouts, so for causal masking
+// the allowed keys of a row are a prefix of each KV shard, the allowed queries
+// of a key a suffix of each Q shard, and a tile is empty, full or partial by
+// its corners.  Varlen (contiguous layout, one cu_seqlens) adds the segment
+// bounds.  P is any parameter struct with N, L, layout, causal, cu and n_seqs.
+#pragma once
+
+#include "ra_internal.h"
+
+namespace ra {
+
+// Query rows [i0, i0 + rows) of Q shard r; the valid ones end at i_last.
+struct QRange {
+  int r, i0, i_last;
+  int gq_lo, gq_hi;    // original token indices of the first / last valid row
+  int key_lo, key_hi;  // varlen: keys any row may see (inclusive)
+  int seg_single;      // varlen: the segment of every valid row, or -1
+};
+
+template <class P>
+__device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows, QRange& q) {
+  q.r = r;
+  q.i0 = i0;
+  q.i_last = min(i0 + rows, p.L) - 1;
+  const int ilo = min(i0, p.L - 1);
+  q.gq_lo = token_of(p.layout, p.N, p.L, r, ilo);
+  q.gq_hi = token_of(p.layout, p.N, p.L, r, max(q.i_last, ilo));
+  q.key_lo = q.key_hi = 0;
+  q.seg_single = -1;
+  if (p.cu) {
+    const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
+    const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
+    q.key_lo = __ldg(p.cu + sa);
+    q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
+    q.seg_single = sa == sz ? sa : -1;
+  }
+}
+
+// Key-tile range [lo, hi) of KV shard s that can hold a key allowed for some row of q.
+template <class P>
+__device__ __forceinline__ void kv_range(const P& p, const QRange& q, int s, int nkt, int& lo, int& hi) {
+  if (p.cu) {
+    const int base = s * p.L;
+    int jlo = q.key_lo - base, jhi = q.key_hi - base;
+    if (jlo < 0) jlo = 0;
+    if (jhi > p.L - 1) jhi = p.L - 1;
+    if (jlo > jhi) {
+      lo = hi = 0;
+      return;
+    }
+    lo = jlo / kTileN;
+    hi = jhi / kTileN + 1;
+    return;
+  }
+  lo = 0;
+  if (!p.causal) {
+    hi = nkt;
+    return;
+  }
+  // the allowed keys of the largest row token are a prefix of the shard and
+  // cover every other row's keys
+  const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, q.gq_hi);
+  hi = jm < 0 ? 0 : jm / kTileN + 1;
+}
+
+// True when every (valid row of q, key) pair of key tile kt of shard s is allowed.
+template <class P>
+__device__ __forceinline__ bool kv_tile_full(const P& p, const QRange& q, int s, int kt) {
+  const int j0 = kt * kTileN;
+  if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
+  if (p.cu) {
+    if (q.seg_single < 0) return false;
+    const int base = s * p.L + j0;
+    const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
+    if (base < slo || base + kTileN > shi) return false;
+    return !p.causal || q.gq_lo >= base + kTileN - 1;
+  }
+  return !p.causal || q.gq_lo >= token_of(p.layout, p.N, p.L, s, j0 + kTileN - 1);
+}
+
+// Calls f(s, kt) for every key tile the rows of q meet at ring steps [t0, t1).
+template <class P, class F>
+__device__ __forceinline__ void walk_kv_tiles(const P& p, const QRange& q, int nkt, int t0, int t1, F&& f) {
+  for (int t = t0; t < t1; ++t) {
+    int s = q.r - t;
+    if (s < 0) s += p.N;
+    int lo, hi;
+    kv_range(p, q, s, nkt, lo, hi);
+    for (int kt = lo; kt < hi; ++kt)
+      if (!f(s, kt)) return;
+  }
+}
+
+// Allowed key columns [c_lo, c_hi) of a query row (token gq, varlen key bounds
+// [rk_lo, rk_hi)) in key tile kt of shard s.
+template <class P>
+__device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, int rk_hi, int s, int kt, int& c_lo,
+                                               int& c_hi) {
+  const int j0 = kt * kTileN;
+  const int jlim = min(kTileN, p.L - j0);
+  c_lo = 0;
+  c_hi = jlim;
+  if (p.cu) {
+    const int base = s * p.L + j0;
+    const int lo = rk_lo - base, hi = rk_hi - base;
+    c_lo = lo < 0 ? 0 : (lo > kTileN ? kTileN : lo);
+    c_hi = hi < 0 ? 0 : (hi > jlim ? jlim : hi);
+  } else if (p.causal) {
+    const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, gq);
+    c_hi = min(jlim, jm - j0 + 1);
+  }
+}
+
+// Key rows [j0, j0 + 128) of KV shard s.
+struct KRange {
+  int s, j0, j_last;
+  int gk_lo, gk_hi;
+  int qry_lo, qry_hi;  // varlen: queries any key of the tile may serve (inclusive)
+  int seg_single;
+};
+
+template <class P>
+__device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k) {
+  k.s = s;
+  k.j0 = j0;
+  k.j_last = min(j0 + kTileN, p.L) - 1;
+  k.gk_lo = token_of(p.layout, p.N, p.L, s, j0);
+  k.gk_hi = token_of(p.layout, p.N, p.L, s, k.j_last);
+  k.qry_lo = k.qry_hi = 0;
+  k.seg_single = -1;
+  if (p.cu) {
+    const int sa = segment_of(p.cu, p.n_seqs, k.gk_lo);
+    const int sz = segment_of(p.cu, p.n_seqs, k.gk_hi);
+    k.qry_lo = p.causal ? k.gk_lo : __ldg(p.cu + sa);
+    k.qry_hi = __ldg(p.cu + sz + 1) - 1;
+    k.seg_single = sa == sz ? sa : -1;
+  }
+}
+
+// Query-tile range [lo, hi) of Q shard r that holds a query some key of k serves.
+template <class P>
+__device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int nqt, int& lo, int& hi) {
+  if (p.cu) {
+    const int base = r * p.L;
+    int ilo = k.qry_lo - base, ihi = k.qry_hi - base;
+    if (ilo < 0) ilo = 0;
+    if (ihi > p.L - 1) ihi = p.L - 1;
+    if (ilo > ihi) {
+      lo = hi = 0;
+      return;
+    }
+    lo = ilo / kTileM;
+    hi = ihi / kTileM + 1;
+    return;
+  }
+  hi = nqt;
+  if (!p.causal) {
+    lo = 0;
+    return;
+  }
+  // first local query of shard r whose token is >= the tile's first key token
+  const int imin = last_local_at_or_before(p.layout, p.N, p.L, r, k.gk_lo - 1) + 1;
+  lo = imin >= p.L ? nqt : imin / kTileM;
+}
+
+// True when every (key of k, valid query) pair of query tile qt of shard r is allowed.
+template <class P>
+__device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, int qt) {
+  const int i0 = qt * kTileM;
+  if (i0 + kTileM > p.L || k.j0 + kTileN > p.L) return false;
+  if (p.cu) {
+    if (k.seg_single < 0) return false;
+    const int base = r * p.L + i0;
+    const int slo = __ldg(p.cu + k.seg_single), shi = __ldg(p.cu + k.seg_single + 1);
+    if (base < slo || base + kTileM > shi) return false;
+    return !p.causal || base >= k.gk_hi;
+  }
+  return !p.causal || token_of(p.layout, p.N, p.L, r, i0) >= k.gk_hi;
+}
+
+// Calls f(r, qt) for every query tile the keys of k serve, in ring order.
+template <class P, class F>
+__device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nqt, F&& f) {
+  for (int t = 0; t < p.N; ++t) {
+    int r = k.s + t;
+    if (r >= p.N) r -= p.N;
+    int lo, hi;
+    q_range(p, k, r, nqt, lo, hi);
+    for (int qt = lo; qt < hi; ++qt)
+      if (!f(r, qt)) return;
+  }
+}
+
+// Allowed query columns [c_lo, c_hi) of a key row (token gk, varlen query bounds
+// [rq_lo, rq_hi)) in query tile qt of shard r.
+template <class P>
+__device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int gk, int rq_lo, int rq_hi, int r, int qt,
+                                                 int& c_lo, int& c_hi) {
+  c_lo = c_hi = 0;
+  if (!valid_k) return;
+  const int i0 = qt * kTileM;
+  const int ilim = min(kTileM, p.L - i0);
+  c_hi = ilim;
+  if (p.cu) {
+    const int base = r * p.L + i0;
+    const int lo = rq_lo - base, hi = rq_hi - base;
+    c_lo = lo < 0 ? 0 : (lo > kTileM ? kTileM : lo);
+    c_hi = hi < 0 ? 0 : (hi > ilim ? ilim : hi);
+  } else if (p.causal) {
+    const int imin = last_local_at_or_before(p.layout, p.N, p.L, r, gk - 1) + 1;
+    c_lo = max(0, imin - i0);
+  }
+}
+
+}  // namespace ra

@@ -47,11 +47,10 @@ def test_status_strings_and_version(lib):
 def test_workspace_size(lib):
     assert lib.ring_attn_workspace_size(0, 1, 2, 256, 64, 2) == 0
     r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    acc = 1 * 2 * 256 * 64 * 4
-    # 2 shards of 128 rows: no padding
-    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 2) == r256(acc) + 2 * r256(1 * 2 * 2 * 128 * 4)
+    # 2 shards of 128 rows: no padding; D and lse2, one float per row each
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 2) == 2 * r256(1 * 2 * 2 * 128 * 4)
     # 4 shards of 64 rows: each padded to 128
-    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 4) == r256(acc) + 2 * r256(1 * 2 * 4 * 128 * 4)
+    assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 4) == 2 * r256(1 * 2 * 4 * 128 * 4)
     assert lib.ring_attn_workspace_size(1, 0, 2, 256, 64, 2) == 0
     assert lib.ring_attn_workspace_size(1, 1, 2, 256, 64, 3) == 0
 
