@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
 SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_simple.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("ra_device.cuh", "ra_internal.h")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("ra_device.cuh", "ra_internal.h", "ra_tiles.cuh")] + [
     os.path.join(ROOT, "include", "ringattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

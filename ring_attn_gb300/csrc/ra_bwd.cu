@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   KRange k;
   make_krange(p, (int)blockIdx.x / p.n_ktiles, ((int)blockIdx.x % p.n_ktiles) * kTileN, k);
   int n_tiles = 0;
-  walk_q_tiles(p, k, p.n_qtiles, [&](int, int) {
+  walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
     ++n_tiles;
     return true;
   });
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
       }
       int i = 0;
-      walk_q_tiles(p, k, p.n_qtiles, [&](int r, int qt) {
+      walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
         const int st = i & 1;
         if (i >= 2 && !wait_one(BAR(E_QDO_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.ctl, 31)) return false;
         const int qrow = r * p.L + qt * kTileM;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_one(BAR(E_KV_FULL), 0, abort_flag, p.ctl, 32);
       int i = 0;
       if (ok) {
-        walk_q_tiles(p, k, p.n_qtiles, [&](int, int) {
+        walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
           const int st = i & 1;
           const uint32_t qb = sb + LY::kQ + st * LY::kTile, ob = sb + LY::kDO + st * LY::kTile;
           if (!wait_one(BAR(E_QDO_FULL + st), (i >> 1) & 1, abort_flag, p.ctl, 33)) {
@@ -272,11 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool ok = true;
     int i = 0;
-    walk_q_tiles(p, k, p.n_qtiles, [&](int r, int qt) {
+    walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
       const int st = i & 1;
       // padding query rows have lse2 = +inf and D = 0 (P = 0, dS = 0) without a mask
       int c_lo = 0, c_hi = kTileM;
-      if (!q_tile_full(p, k, r, qt)) key_query_window(p, valid_k, gk, rq_lo, rq_hi, r, qt, c_lo, c_hi);
+      if (!q_tile_full<kTileM>(p, k, r, qt)) key_query_window<kTileM>(p, valid_k, gk, rq_lo, rq_hi, r, qt, c_lo, c_hi);
       c_lo -= 64 * half;
       c_hi -= 64 * half;
       const bool masked = c_lo > 0 || c_hi < 64;

@@ -143,8 +143,8 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
   }
 }
 
-// Query-tile range [lo, hi) of Q shard r that holds a query some key of k serves.
-template <class P>
+// Query-tile range [lo, hi) (tiles of QT rows) of Q shard r that holds a query some key of k serves.
+template <int QT, class P>
 __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int nqt, int& lo, int& hi) {
   if (p.cu) {
     const int base = r * p.L;
@@ -155,8 +155,8 @@ __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int 
       lo = hi = 0;
       return;
     }
-    lo = ilo / kTileM;
-    hi = ihi / kTileM + 1;
+    lo = ilo / QT;
+    hi = ihi / QT + 1;
     return;
   }
   hi = nqt;
@@ -166,51 +166,51 @@ __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int 
   }
   // first local query of shard r whose token is >= the tile's first key token
   const int imin = last_local_at_or_before(p.layout, p.N, p.L, r, k.gk_lo - 1) + 1;
-  lo = imin >= p.L ? nqt : imin / kTileM;
+  lo = imin >= p.L ? nqt : imin / QT;
 }
 
-// True when every (key of k, valid query) pair of query tile qt of shard r is allowed.
-template <class P>
+// True when every (key of k, valid query) pair of query tile qt (QT rows) of shard r is allowed.
+template <int QT, class P>
 __device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, int qt) {
-  const int i0 = qt * kTileM;
-  if (i0 + kTileM > p.L || k.j0 + kTileN > p.L) return false;
+  const int i0 = qt * QT;
+  if (i0 + QT > p.L || k.j0 + kTileN > p.L) return false;
   if (p.cu) {
     if (k.seg_single < 0) return false;
     const int base = r * p.L + i0;
     const int slo = __ldg(p.cu + k.seg_single), shi = __ldg(p.cu + k.seg_single + 1);
-    if (base < slo || base + kTileM > shi) return false;
+    if (base < slo || base + QT > shi) return false;
     return !p.causal || base >= k.gk_hi;
   }
   return !p.causal || token_of(p.layout, p.N, p.L, r, i0) >= k.gk_hi;
 }
 
-// Calls f(r, qt) for every query tile the keys of k serve, in ring order.
-template <class P, class F>
+// Calls f(r, qt) for every query tile (QT rows) the keys of k serve, in ring order.
+template <int QT, class P, class F>
 __device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nqt, F&& f) {
   for (int t = 0; t < p.N; ++t) {
     int r = k.s + t;
     if (r >= p.N) r -= p.N;
     int lo, hi;
-    q_range(p, k, r, nqt, lo, hi);
+    q_range<QT>(p, k, r, nqt, lo, hi);
     for (int qt = lo; qt < hi; ++qt)
       if (!f(r, qt)) return;
   }
 }
 
 // Allowed query columns [c_lo, c_hi) of a key row (token gk, varlen query bounds
-// [rq_lo, rq_hi)) in query tile qt of shard r.
-template <class P>
+// [rq_lo, rq_hi)) in query tile qt (QT rows) of shard r.
+template <int QT, class P>
 __device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int gk, int rq_lo, int rq_hi, int r, int qt,
                                                  int& c_lo, int& c_hi) {
   c_lo = c_hi = 0;
   if (!valid_k) return;
-  const int i0 = qt * kTileM;
-  const int ilim = min(kTileM, p.L - i0);
+  const int i0 = qt * QT;
+  const int ilim = min(QT, p.L - i0);
   c_hi = ilim;
   if (p.cu) {
     const int base = r * p.L + i0;
     const int lo = rq_lo - base, hi = rq_hi - base;
-    c_lo = lo < 0 ? 0 : (lo > kTileM ? kTileM : lo);
+    c_lo = lo < 0 ? 0 : (lo > QT ? QT : lo);
     c_hi = hi < 0 ? 0 : (hi > ilim ? ilim : hi);
   } else if (p.causal) {
     const int imin = last_local_at_or_before(p.layout, p.N, p.L, r, gk - 1) + 1;
