@@ -66,7 +66,8 @@ typedef enum {
   RA_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than ring_attn_workspace_size */
   RA_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
   RA_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (see check_device_error) */
-  RA_ERR_DEVICE = 7       /* other device-side error (e.g. misaligned shared memory) */
+  RA_ERR_DEVICE = 7,      /* other device-side error (e.g. misaligned shared memory) */
+  RA_ERR_SCRATCH_LIMIT = 8 /* the problem needs more than the library's static scratch holds */
 } ra_status;
 
 typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype;
@@ -133,6 +134,36 @@ ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tens
                         const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
                         int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ring_attn_bwd_static_scratch: ring_attn_bwd without a caller workspace.
+ * The pages have no counterpart: it is a library convenience for callers that
+ * cannot hand over device memory, e.g. an integration point whose signature
+ * has no workspace argument, or a process whose device memory is already
+ * fully reserved by another allocator, so that allocating at that point would
+ * fail.  It allocates nothing: the per-row statistics (D and lse * log2(e))
+ * live in one array of RA_STATIC_SCRATCH_BYTES bytes that the library holds
+ * in device memory on every device that loads it, until the process exits (a
+ * file-scope __device__ array).
+ *   Arguments, layouts and results are those of ring_attn_bwd.
+ *   Limit: ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards) must not
+ *   exceed RA_STATIC_SCRATCH_BYTES (16 MiB: up to 2,097,152 query rows after
+ *   padding each shard to a multiple of 128, e.g. b = 1, h = 32, s = 65536),
+ *   else RA_ERR_SCRATCH_LIMIT is returned before any launch.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   with that device current (cudaGetSymbolAddress, which loads the library's
+ *   device code if it is not loaded yet); make that first call before any
+ *   stream capture begins.  Later calls on the device reuse the address.
+ *   The array keeps the last call's contents; nothing in it needs to start at
+ *   zero, because every call writes all of it that it reads before reading it.
+ *   Races: every call on a device shares the array.  Calls ordered on one
+ *   stream are safe; two calls that can run on the GPU at the same time
+ *   (different streams without ordering between them, or other host threads)
+ *   race on it and give wrong gradients. */
+#define RA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k,
+                                       const ra_tensor* v, const ra_tensor* out, const ra_tensor* lse,
+                                       int32_t layout, int32_t n_shards, int32_t causal, float softmax_scale,
+                                       ra_tensor* dq, ra_tensor* dk, ra_tensor* dv, void* stream);
 
 /* Varlen (packed) forms ([README] API list, "the varlen versions only support
  * passing one cu_seqlens").  q, k, v, out: 3-D (total, h, d) or (h, total, d)

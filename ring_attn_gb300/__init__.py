@@ -18,7 +18,8 @@ __all__ = [
     "LAYOUTS", "RingAttnError", "lib_path", "load", "ring_attn_fwd", "ring_attn_fwd_step", "ring_attn_bwd",
     "ring_attn_varlen_fwd", "ring_attn_varlen_bwd", "lse_merge", "ring_attn_permute", "ring_attn_unpermute",
     "ring_attn_workspace_size", "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_version",
-    "ring_attn_timing_enable", "ring_attn_timing_read", "EXPORTED_SYMBOLS", "KERNELS",
+    "ring_attn_timing_enable", "ring_attn_timing_read", "ring_attn_bwd_static_scratch", "EXPORTED_SYMBOLS",
+    "KERNELS", "RA_STATIC_SCRATCH_BYTES",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -31,8 +32,9 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_step", "lse_merge", "ring_attn_bwd", "ring_attn_varlen_fwd",
     "ring_attn_varlen_bwd", "ring_attn_permute", "ring_attn_unpermute", "ring_attn_workspace_size",
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
-    "ra_status_string", "ring_attn_version",
+    "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch",
 )
+RA_STATIC_SCRATCH_BYTES = 16 << 20
 KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
 
 
@@ -71,6 +73,7 @@ def load():
         "ring_attn_fwd_step": [T, T, T, I32, I32, I32, F32, I32, T, T, P],
         "lse_merge": [T, T, T, T, P],
         "ring_attn_bwd": [T, T, T, T, T, T, I32, I32, I32, F32, T, T, T, P, SZ, P],
+        "ring_attn_bwd_static_scratch": [T, T, T, T, T, T, I32, I32, I32, F32, T, T, T, P],
         "ring_attn_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, F32, T, T, P, SZ, P],
         "ring_attn_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
         "ring_attn_permute": [T, T, I32, I32, I32, P],
@@ -202,6 +205,25 @@ def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, caus
     _check(lib.ring_attn_bwd(r[0], r[1], r[2], r[3], r[4], r[5], _layout(layout), int(n_shards), int(bool(causal)),
                              _scale(softmax_scale, d), r[6], r[7], r[8], ctypes.c_void_p(workspace.data_ptr()),
                              workspace.numel() * workspace.element_size(), _stream(stream)), "ring_attn_bwd")
+    return dq, dk, dv
+
+
+def ring_attn_bwd_static_scratch(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, causal=False,
+                                 softmax_scale=None, dq=None, dk=None, dv=None, stream=None):
+    """ring_attn_bwd with the library's static device scratch instead of a workspace.
+
+    The library call allocates nothing; only the outputs this wrapper creates when
+    dq, dk or dv is None are allocated here, so callers that cannot allocate pass
+    all three.  Calls that may overlap on the GPU race on the shared scratch."""
+    lib = load()
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    r = [ctypes.byref(x) for x in ts]
+    _check(lib.ring_attn_bwd_static_scratch(r[0], r[1], r[2], r[3], r[4], r[5], _layout(layout), int(n_shards),
+                                            int(bool(causal)), _scale(softmax_scale, q.shape[-1]), r[6], r[7], r[8],
+                                            _stream(stream)), "ring_attn_bwd_static_scratch")
     return dq, dk, dv
 
 

@@ -321,6 +321,12 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   return cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 1, st));
 }
 
+// Scratch of ring_attn_bwd_static_scratch: one array per device, its device
+// address looked up once per device (with that device current) and cached.
+void* g_scratch_ptr[64] = {nullptr};
+
+ra_status static_scratch(void** out);
+
 ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs, int32_t max_seqlen,
                    long long* total) {
   if (!cu_dev || !cu_host || n_seqs < 1) return RA_ERR_INVALID_ARG;
@@ -335,6 +341,28 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
   if (max_seqlen < mx) return RA_ERR_INVALID_ARG;
   *total = cu_host[n_seqs];
   if (*total < 1) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+}  // namespace
+
+// Statistics of ring_attn_bwd_static_scratch (D, then lse * log2(e)).  The
+// library never allocates it: it is part of the loaded device image.  In host
+// code this name is only a stand-in; static_scratch gives the device address.
+static __device__ __align__(256) unsigned char g_bwd_scratch[RA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+ra_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return RA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
   return RA_OK;
 }
 
@@ -482,6 +510,29 @@ ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tens
   RA_TRY(check_lse(lse, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k,
+                                       const ra_tensor* v, const ra_tensor* out, const ra_tensor* lse,
+                                       int32_t layout, int32_t n_shards, int32_t causal, float softmax_scale,
+                                       ra_tensor* dq, ra_tensor* dk, ra_tensor* dv, void* stream) {
+  Bhsd vdo, vq, vk, vv, vo, vdq, vdk, vdv;
+  RA_TRY(check_bhsd(dout, &vdo));
+  RA_TRY(check_bhsd(q, &vq));
+  RA_TRY(check_bhsd(k, &vk));
+  RA_TRY(check_bhsd(v, &vv));
+  RA_TRY(check_bhsd(out, &vo));
+  RA_TRY(check_bhsd(dq, &vdq));
+  RA_TRY(check_bhsd(dk, &vdk));
+  RA_TRY(check_bhsd(dv, &vdv));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
+  RA_TRY(check_layout(layout, n_shards, vq.s));
+  if (bwd_ws_bytes(vq.b, vq.h, vq.s, n_shards) > RA_STATIC_SCRATCH_BYTES) return RA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  RA_TRY(static_scratch(&scratch));
+  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
+                    causal, softmax_scale, vdq, vdk, vdv, scratch, RA_STATIC_SCRATCH_BYTES, nullptr, 0, stream);
 }
 
 ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
@@ -655,6 +706,7 @@ const char* ra_status_string(int32_t status) {
     case RA_ERR_CUDA: return "CUDA runtime error";
     case RA_ERR_TIMEOUT: return "a bounded device-side wait ran out";
     case RA_ERR_DEVICE: return "device-side error";
+    case RA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static array holds";
     default: return "unknown status";
   }
 }
