@@ -80,11 +80,18 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, bool v
 }
 
 // ======================================================================== dK / dV
-// Warps: 0 TMA (K, V once; Q, dO and the query tile's lse2 / D into a 2-stage
-// ring), 1 MMA, 2 TMEM; warpgroups 1 and 2: one key row each, columns [0, 64)
-// and [64, 128).  TMEM: S^T [0,128) (then P^T), dP^T [128,256) (then dS^T),
-// dV [256, 256+D), dK [256+D, 256+2D).  Per query tile: S^T, dP^T, then once
-// P^T and dS^T are in TMEM, dV += P^T dO and dK += dS^T Q (A operands from TMEM).
+// Warps: 0 TMA (K, V once; Q with the query tile's lse2 / D, and dO, into two
+// 2-stage rings), 1 MMA, 2 TMEM; warpgroups 1 and 2: one key row each, query
+// columns [0, 64) and [64, 128).  TMEM: S^T [0,128), dP^T [128,256), dV
+// [256, 256+D), dK [256+D, 256+2D).  A thread reads its 64 S^T columns into
+// registers and releases them at once, so S^T of the next query tile can be
+// computed while this one is processed; it then writes P^T and dS^T as packed
+// bf16 over its own 64 dP^T columns (P^T in the first 32, dS^T in the last 32),
+// the A operands of dV += P^T dO and dK += dS^T Q.  Per query tile i the MMA
+// thread issues
+//   S^T(i+1) [once S^T(i) is read], dK(i), dV(i) [once P^T, dS^T are in TMEM],
+//   dP^T(i+1)
+// (dK first: it frees the Q stage the next-but-one S^T needs).
 template <int D>
 struct DkdvLayout {
   static constexpr int kTile = (D / 64) * kBox;
@@ -92,9 +99,9 @@ struct DkdvLayout {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;          // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;     // 2 stages
-  static constexpr int kStats = kDO + 2 * kTile; // 2 stages x (lse2, D), 128 floats each
+  static constexpr int kStats = kDO + 2 * kTile; // 2 stages (with Q) x (lse2, D), 128 floats each
   static constexpr int kBar = kStats + 2 * 2 * 512;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 15;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
@@ -102,13 +109,16 @@ struct DkdvLayout {
 
 enum DkdvBar {
   E_KV_FULL = 0,
-  E_QDO_FULL = 1,   // 2
-  E_QDO_EMPTY = 3,  // 2
-  E_S_FULL = 5,
-  E_DP_FULL = 6,
-  E_PS_FULL = 7,    // P^T and dS^T in TMEM: 8 elected arrivals
-  E_KV_DONE = 8,
-  E_TEARDOWN = 9
+  E_Q_FULL = 1,     // 2: Q, lse2 and D of a query tile
+  E_Q_EMPTY = 3,    // 2
+  E_DO_FULL = 5,    // 2
+  E_DO_EMPTY = 7,   // 2
+  E_S_FULL = 9,
+  E_S_READ = 10,    // S^T in registers: 8 elected arrivals
+  E_DP_FULL = 11,
+  E_PS_FULL = 12,   // P^T and dS^T in TMEM: 8 elected arrivals
+  E_KV_DONE = 13,
+  E_TEARDOWN = 14
 };
 
 template <int D>
@@ -140,10 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(E_KV_FULL), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(E_QDO_FULL + i), 1);
-      mbar_init(BAR(E_QDO_EMPTY + i), 1);
+      mbar_init(BAR(E_Q_FULL + i), 1);
+      mbar_init(BAR(E_Q_EMPTY + i), 1);
+      mbar_init(BAR(E_DO_FULL + i), 1);
+      mbar_init(BAR(E_DO_EMPTY + i), 1);
     }
     mbar_init(BAR(E_S_FULL), 1);
+    mbar_init(BAR(E_S_READ), 8);
     mbar_init(BAR(E_DP_FULL), 1);
     mbar_init(BAR(E_PS_FULL), 8);
     mbar_init(BAR(E_KV_DONE), 1);
@@ -180,24 +193,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = 0;
       walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
         const int st = i & 1;
-        if (i >= 2 && !wait_one(BAR(E_QDO_EMPTY + st), ((i >> 1) - 1) & 1, abort_flag, p.ctl, 31)) return false;
+        const uint32_t par = ((i >> 1) - 1) & 1;
         const int qrow = r * p.L + qt * kTileM;
+        if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) return false;
         // lse2 / D of the tile's 128 query rows: 512-byte aligned in the padded layout
         const long long e0 = stat_bh + (long long)r * p.stat_L + qt * kTileM;
-        mbar_expect_tx(BAR(E_QDO_FULL + st), 2 * LY::kTile + 2 * 512);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_QDO_FULL + st), c * 64, qrow, h, b);
-          tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_QDO_FULL + st), c * 64, qrow, h, b);
+        mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
+        bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.lse2 + e0, 512, BAR(E_Q_FULL + st));
+        bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.Dsum + e0, 512, BAR(E_Q_FULL + st));
+        if (i >= 2 && !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)) {
+          drain_one(BAR(E_Q_FULL + st), (i >> 1) & 1, p.ctl, 43);
+          return false;
         }
-        bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.lse2 + e0, 512, BAR(E_QDO_FULL + st));
-        bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.Dsum + e0, 512, BAR(E_QDO_FULL + st));
+        mbar_expect_tx(BAR(E_DO_FULL + st), LY::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_DO_FULL + st), c * 64, qrow, h, b);
         ++issued[st];
         ++i;
         return true;
       });
       drain_one(BAR(E_KV_FULL), 0, p.ctl, 40);
       for (int st = 0; st < 2; ++st)
-        if (issued[st]) drain_one(BAR(E_QDO_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
+        if (issued[st]) {
+          drain_one(BAR(E_Q_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
+          drain_one(BAR(E_DO_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
+        }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -205,52 +227,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, kTileM, 0, 0);  // S^T, dP^T: K-major A and B
       constexpr uint32_t kIdKV = idesc_bf16_f32(128, D, 0, 1);      // dV, dK: TMEM A, MN-major B
-      bool ok = wait_one(BAR(E_KV_FULL), 0, abort_flag, p.ctl, 32);
-      int i = 0;
+      // X^T = A B^T over D: A (K or V) and B (Q or dO tile) K-major in shared memory
+      auto issue_t = [&](uint32_t dcol, uint32_t a, uint32_t bq) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_bf16_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024), kIdS,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = wait_one(BAR(E_KV_FULL), 0, abort_flag, p.ctl, 32) &&
+                wait_one(BAR(E_Q_FULL), 0, abort_flag, p.ctl, 33);
       if (ok) {
-        walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
-          const int st = i & 1;
-          const uint32_t qb = sb + LY::kQ + st * LY::kTile, ob = sb + LY::kDO + st * LY::kTile;
-          if (!wait_one(BAR(E_QDO_FULL + st), (i >> 1) & 1, abort_flag, p.ctl, 33)) {
-            ok = false;
-            return false;
-          }
+        tc_fence_after();
+        issue_t(LY::kTmemS, sb + LY::kK, sb + LY::kQ);
+        mma_commit(BAR(E_S_FULL));
+        ok = wait_one(BAR(E_DO_FULL), 0, abort_flag, p.ctl, 34);
+        if (ok) {
           tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T; their columns held P^T / dS^T of the previous
-          // tile, already read by the dV / dK MMAs issued before these
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + LY::kTmemS, sdesc_sw128(sb + LY::kK + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                        kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(BAR(E_S_FULL));
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + LY::kTmemDP, sdesc_sw128(sb + LY::kV + off, 16, 1024), sdesc_sw128(ob + off, 16, 1024),
-                        kIdS, kk > 0 ? 1u : 0u);
-          }
+          issue_t(LY::kTmemDP, sb + LY::kV, sb + LY::kDO);
           mma_commit(BAR(E_DP_FULL));
-          if (!wait_one(BAR(E_PS_FULL), i & 1, abort_flag, p.ctl, 35)) {
+        }
+      }
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int st = i & 1, st1 = (i + 1) & 1;
+        const uint32_t par1 = ((i + 1) >> 1) & 1;
+        if (i + 1 < n_tiles) {
+          // S^T(i+1) into the S^T columns once every thread holds S^T(i) in registers
+          if (!wait_one(BAR(E_Q_FULL + st1), par1, abort_flag, p.ctl, 33) ||
+              !wait_one(BAR(E_S_READ), i & 1, abort_flag, p.ctl, 45)) {
             ok = false;
-            return false;
+            break;
           }
           tc_fence_after();
+          issue_t(LY::kTmemS, sb + LY::kK, sb + LY::kQ + st1 * LY::kTile);
+          mma_commit(BAR(E_S_FULL));
+        }
+        if (!wait_one(BAR(E_PS_FULL), i & 1, abort_flag, p.ctl, 35)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qb = sb + LY::kQ + st * LY::kTile, ob = sb + LY::kDO + st * LY::kTile;
+        // dK += dS^T Q, then dV += P^T dO: A from the packed dP^T columns, B with 16 query rows per step
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            // dV += P^T dO and dK += dS^T Q: A from TMEM, B = dO / Q with 16 query rows per step
-            mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemS + pcol(kk), sdesc_sw128(ob + kk * 2048, kBox, 1024),
-                        kIdKV, acc);
-            mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(qb + kk * 2048, kBox, 1024),
-                        kIdKV, acc);
+        for (int kk = 0; kk < kTileM / 16; ++kk)
+          mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk) + 32, sdesc_sw128(qb + kk * 2048, kBox, 1024),
+                      kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 2 < n_tiles) mma_commit(BAR(E_Q_EMPTY + st));
+#pragma unroll
+        for (int kk = 0; kk < kTileM / 16; ++kk)
+          mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(ob + kk * 2048, kBox, 1024),
+                      kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 2 < n_tiles) mma_commit(BAR(E_DO_EMPTY + st));
+        if (i + 1 == n_tiles) {
+          mma_commit(BAR(E_KV_DONE));
+        } else {
+          // dP^T(i+1) overwrites the packed operands the dK / dV MMAs above read first
+          if (!wait_one(BAR(E_DO_FULL + st1), par1, abort_flag, p.ctl, 34)) {
+            ok = false;
+            break;
           }
-          if (i + 2 < n_tiles) mma_commit(BAR(E_QDO_EMPTY + st));
-          if (i + 1 == n_tiles) mma_commit(BAR(E_KV_DONE));
-          ++i;
-          return true;
-        });
+          tc_fence_after();
+          issue_t(LY::kTmemDP, sb + LY::kV, sb + LY::kDO + st1 * LY::kTile);
+          mma_commit(BAR(E_DP_FULL));
+        }
       }
       mma_commit(BAR(E_TEARDOWN));
       drain_one(BAR(E_TEARDOWN), 0, p.ctl, 42);
@@ -284,13 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* ds4 = reinterpret_cast<const float4*>(sp + LY::kStats + (st * 2 + 1) * 512) + 16 * half;
       // waiting on the stage barrier orders this thread's statistics reads after the copy landed
       if (!wait_warp(BAR(E_S_FULL), i & 1, abort_flag, p.ctl, 36) ||
-          !wait_warp(BAR(E_QDO_FULL + st), (i >> 1) & 1, abort_flag, p.ctl, 44)) {
+          !wait_warp(BAR(E_Q_FULL + st), (i >> 1) & 1, abort_flag, p.ctl, 44)) {
         ok = false;
         return false;
       }
       tc_fence_after();
       uint32_t v[64];
       tmem_ld64(tl + LY::kTmemS + 64 * half, v);
+      // S^T is in registers: the MMA thread may compute the next tile's S^T over it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(E_S_READ));
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l = ls4[c4];
@@ -303,23 +348,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : 0u;
       }
-      tmem_st_bf16x64(tl + LY::kTmemS + 64 * half, v);  // P^T over columns this thread has read
       if (!wait_warp(BAR(E_DP_FULL), i & 1, abort_flag, p.ctl, 37)) {
         ok = false;
         return false;
       }
       tc_fence_after();
-      uint32_t dp[64];
-      tmem_ld64(tl + LY::kTmemDP + 64 * half, dp);
+      // dS^T = P^T * (dP^T - D), 32 dP^T columns at a time.  The thread's 64 dP^T
+      // columns then hold P^T packed in [0, 32) (column m: queries 2m, 2m + 1) and
+      // dS^T packed in [32, 64); a packed half is stored once the columns under it are read.
+      const uint32_t tdp = tl + LY::kTmemDP + 64 * half;
+      uint32_t ps[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 dd = ds4[c4];
-        dp[4 * c4 + 0] = __float_as_uint(__uint_as_float(v[4 * c4 + 0]) * (__uint_as_float(dp[4 * c4 + 0]) - dd.x));
-        dp[4 * c4 + 1] = __float_as_uint(__uint_as_float(v[4 * c4 + 1]) * (__uint_as_float(dp[4 * c4 + 1]) - dd.y));
-        dp[4 * c4 + 2] = __float_as_uint(__uint_as_float(v[4 * c4 + 2]) * (__uint_as_float(dp[4 * c4 + 2]) - dd.z));
-        dp[4 * c4 + 3] = __float_as_uint(__uint_as_float(v[4 * c4 + 3]) * (__uint_as_float(dp[4 * c4 + 3]) - dd.w));
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t d[32];
+        tmem_ld32(tdp + 32 * hh, d);
+        tmem_ld_wait(d);
+        uint32_t pp[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dd = ds4[8 * hh + c4];
+          const int c = 32 * hh + 4 * c4;
+          const float p0 = __uint_as_float(v[c]), p1 = __uint_as_float(v[c + 1]);
+          const float p2 = __uint_as_float(v[c + 2]), p3 = __uint_as_float(v[c + 3]);
+          pp[2 * c4] = pack_bf16x2(p0, p1);
+          pp[2 * c4 + 1] = pack_bf16x2(p2, p3);
+          ps[16 * hh + 2 * c4] = pack_bf16x2(p0 * (__uint_as_float(d[4 * c4]) - dd.x),
+                                             p1 * (__uint_as_float(d[4 * c4 + 1]) - dd.y));
+          ps[16 * hh + 2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(d[4 * c4 + 2]) - dd.z),
+                                                 p3 * (__uint_as_float(d[4 * c4 + 3]) - dd.w));
+        }
+        tmem_st16(tdp + 16 * hh, pp);
       }
-      tmem_st_bf16x64(tl + LY::kTmemDP + 64 * half, dp);  // dS^T
+      tmem_st16(tdp + 32, *reinterpret_cast<uint32_t(*)[16]>(ps));
+      tmem_st16(tdp + 48, *reinterpret_cast<uint32_t(*)[16]>(ps + 16));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
