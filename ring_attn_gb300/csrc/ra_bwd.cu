@@ -44,18 +44,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
 }
 
-// 64 fp32 values as 32 packed bf16 pairs at taddr (two 16-column stores).
-__device__ __forceinline__ void tmem_st_bf16x64(uint32_t taddr, const uint32_t (&v)[64]) {
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-      pk[u] = pack_bf16x2(__uint_as_float(v[32 * c + 2 * u]), __uint_as_float(v[32 * c + 2 * u + 1]));
-    tmem_st16(taddr + 16 * c, pk);
-  }
-}
-
 // One bf16 output row segment of N32 * 32 columns from TMEM, times mul.
 template <int N32>
 __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, bool valid, __nv_bfloat16* dst) {
@@ -415,11 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ======================================================================== dQ
 // Warps: 0 TMA (Q, dO once, then K into a 3-stage ring), 3 TMA (V into a
-// 2-stage ring), 1 MMA, 2 TMEM; warpgroups 1 and 2: one query row each,
-// key columns [0, 64) and [64, 128).  TMEM: S [0,256) double-buffered (then dS
-// over it), dP [256,384), dQ [384, 384+D).  Per key tile j the MMA thread issues
-//   S(j+1), dP(j+1) [once dP(j) has been read], dQ += dS(j) K(j) [once dS(j) is in TMEM]
-// so that S and dP of the next tile run while the current one is processed.
+// 2-stage ring), 1 MMA, 2 TMEM; warpgroups 1 and 2: one query row each, key
+// columns [0, 64) and [64, 128).  Q and dO are the same for every key tile, so
+// the softmax threads copy them once into tensor memory (packed bf16) and the
+// S and dP MMAs take them from there: shared memory then feeds only the K and V
+// operands.  TMEM: S [0,128), dP [128,256), Q [256, 256+D/2), dO [256+D/2, 256+D),
+// dQ [384, 384+D).  A thread reads its 64 S columns into registers and releases
+// them at once; it writes dS as packed bf16 over the first 32 of its own 64 dP
+// columns, the A operand of dQ += dS K.  Per key tile j the MMA thread issues
+//   S(j+1) [once S(j) is read], dQ += dS(j) K(j) [once dS(j) is in TMEM], dP(j+1)
+// so S of the next tile and the exponentials of the current one overlap.
 template <int D>
 struct DqLayout {
   static constexpr int kTile = (D / 64) * kBox;
@@ -429,10 +422,10 @@ struct DqLayout {
   static constexpr int kK = kDO + kTile;
   static constexpr int kV = kK + kKStages * kTile;
   static constexpr int kBar = kV + kVStages * kTile;
-  static constexpr int kNumBars = 19;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
-  static constexpr uint32_t kTmemS = 0, kTmemDP = 256, kTmemDQ = 384;
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemQ = 256, kTmemDO = 256 + D / 2, kTmemDQ = 384;
 };
 
 enum DqBar {
@@ -441,14 +434,13 @@ enum DqBar {
   F_K_EMPTY = 4,   // 3
   F_V_FULL = 7,    // 2
   F_V_EMPTY = 9,   // 2
-  F_S_FULL = 11,   // 2
+  F_S_FULL = 11,
+  F_S_READ = 12,   // S in registers: 8 elected arrivals
   F_DP_FULL = 13,
-  F_DP_FREE = 14,  // dP read into registers: 8 elected arrivals
-  F_DS_FULL = 15,  // 2, one per S buffer: dS in TMEM, 8 elected arrivals (two barriers so
-                   // that the softmax, which may finish tile j+1 before the MMA thread
-                   // waits for tile j, can never complete a phase twice ahead)
-  F_DQ_DONE = 17,
-  F_TEARDOWN = 18
+  F_DS_FULL = 14,  // dS in TMEM: 8 elected arrivals
+  F_QDO_TMEM = 15, // Q and dO copied into TMEM: 8 elected arrivals
+  F_DQ_DONE = 16,
+  F_TEARDOWN = 17
 };
 
 template <int D>
@@ -493,11 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(F_V_EMPTY + i), 1);
     }
     mbar_init(BAR(F_S_FULL), 1);
-    mbar_init(BAR(F_S_FULL + 1), 1);
+    mbar_init(BAR(F_S_READ), 8);
     mbar_init(BAR(F_DP_FULL), 1);
-    mbar_init(BAR(F_DP_FREE), 8);
     mbar_init(BAR(F_DS_FULL), 8);
-    mbar_init(BAR(F_DS_FULL + 1), 8);
+    mbar_init(BAR(F_QDO_TMEM), 8);
     mbar_init(BAR(F_DQ_DONE), 1);
     mbar_init(BAR(F_TEARDOWN), 1);
     *abort_flag = 0;
@@ -557,48 +548,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTileN, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTileN, 0, 0);  // S = Q K^T, dP = dO V^T: TMEM A, K-major B
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, D, 0, 1);       // dQ += dS K: TMEM A, MN-major B
-      bool ok = wait_one(BAR(F_QDO_FULL), 0, abort_flag, p.ctl, 55);
+      bool ok = wait_one(BAR(F_QDO_TMEM), 0, abort_flag, p.ctl, 55);
+      // X = A B^T over D with A (Q or dO) packed in TMEM, 16 head-dim columns = 8 TMEM columns per step
+      auto issue_t = [&](uint32_t dcol, uint32_t acol, uint32_t bt) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_bf16_ts(tmem + dcol, tmem + acol + 8 * kk, sdesc_sw128(bt + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
       auto issue_s = [&](int j) -> bool {
         const int ks = j % KS;
         if (!wait_one(BAR(F_K_FULL + ks), (j / KS) & 1, abort_flag, p.ctl, 56)) return false;
+        if (j > 0 && !wait_one(BAR(F_S_READ), (j - 1) & 1, abort_flag, p.ctl, 57)) return false;
         tc_fence_after();
-        const uint32_t kb = sb + LY::kK + ks * LY::kTile;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + LY::kTmemS + 128 * (j & 1), sdesc_sw128(sb + LY::kQ + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(BAR(F_S_FULL + (j & 1)));
+        issue_t(LY::kTmemS, LY::kTmemQ, sb + LY::kK + ks * LY::kTile);
+        mma_commit(BAR(F_S_FULL));
         return true;
       };
+      // dP(j) overwrites dS(j-1), which the dQ MMA issued before it has read
       auto issue_dp = [&](int j) -> bool {
         const int vs = j % VS;
-        if (j > 0 && !wait_one(BAR(F_DP_FREE), (j - 1) & 1, abort_flag, p.ctl, 57)) return false;
         if (!wait_one(BAR(F_V_FULL + vs), (j / VS) & 1, abort_flag, p.ctl, 58)) return false;
         tc_fence_after();
-        const uint32_t vb = sb + LY::kV + vs * LY::kTile;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + LY::kTmemDP, sdesc_sw128(sb + LY::kDO + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024),
-                      kIdS, kk > 0 ? 1u : 0u);
-        }
+        issue_t(LY::kTmemDP, LY::kTmemDO, sb + LY::kV + vs * LY::kTile);
         mma_commit(BAR(F_DP_FULL));
         if (j + VS < n_tiles) mma_commit(BAR(F_V_EMPTY + vs));
         return true;
       };
       auto issue_dq = [&](int j) -> bool {
-        if (!wait_one(BAR(F_DS_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.ctl, 59)) return false;
+        if (!wait_one(BAR(F_DS_FULL), j & 1, abort_flag, p.ctl, 59)) return false;
         tc_fence_after();
         const uint32_t kb = sb + LY::kK + (j % KS) * LY::kTile;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          // A = dS (16 keys = 8 packed columns of the S buffer), B = K with 16 key rows per step
-          mma_bf16_ts(tmem + LY::kTmemDQ, tmem + LY::kTmemS + 128 * (j & 1) + pcol(kk),
-                      sdesc_sw128(kb + kk * 2048, kBox, 1024), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+          // A = dS (16 keys = 8 packed columns of the dP region), B = K with 16 key rows per step
+          mma_bf16_ts(tmem + LY::kTmemDQ, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(kb + kk * 2048, kBox, 1024),
+                      kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
         }
         if (j + KS < n_tiles) mma_commit(BAR(F_K_EMPTY + j % KS));
         return true;
@@ -607,9 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         ok = issue_s(0) && issue_dp(0);
         for (int j = 0; ok && j < n_tiles; ++j) {
-          // S(j+1) goes into the buffer whose dS(j-1) the dQ MMA issued before has read
-          if (j + 1 < n_tiles) ok = issue_s(j + 1) && issue_dp(j + 1);
+          if (j + 1 < n_tiles) ok = issue_s(j + 1);
           ok = ok && issue_dq(j);
+          if (ok && j + 1 < n_tiles) ok = issue_dp(j + 1);
         }
         if (ok) mma_commit(BAR(F_DQ_DONE));
       }
@@ -635,22 +623,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long srow = (((long long)b * p.H + h) * p.N + r) * p.stat_L + i;
     const float lse2 = __ldg(p.lse2 + srow);
     const float Drow = __ldg(p.Dsum + srow);
-    bool ok = true;
+    // warpgroup 1 copies the row's Q, warpgroup 2 its dO, into tensor memory as
+    // packed bf16 (column m: head-dim elements 2m, 2m + 1) for the S and dP MMAs
+    bool ok = n_tiles == 0 || wait_warp(BAR(F_QDO_FULL), 0, abort_flag, p.ctl, 64);
+    if (ok && n_tiles > 0) {
+      const uint8_t* src = sp + (half == 0 ? LY::kQ : LY::kDO);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          // 128-byte swizzle: 16-byte chunk q of row `row` sits at chunk q ^ (row & 7)
+          const uint4 x = *reinterpret_cast<const uint4*>(src + c * kBox + row * 128 + ((q ^ (row & 7)) << 4));
+          w[4 * q] = x.x;
+          w[4 * q + 1] = x.y;
+          w[4 * q + 2] = x.z;
+          w[4 * q + 3] = x.w;
+        }
+        tmem_st32(tl + (half == 0 ? LY::kTmemQ : LY::kTmemDO) + 32 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(F_QDO_TMEM));
+    }
     int j = 0;
-    walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int s, int kt) {
-      const uint32_t tS = tl + LY::kTmemS + 128 * (j & 1) + 64 * half;
+    if (ok) walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int s, int kt) {
       int c_lo = 0, c_hi = kTileN;
       if (!kv_tile_full(p, qr, s, kt)) row_key_window(p, gq, rk_lo, rk_hi, s, kt, c_lo, c_hi);
       c_lo -= 64 * half;
       c_hi -= 64 * half;
       const bool masked = c_lo > 0 || c_hi < 64;
-      if (!wait_warp(BAR(F_S_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.ctl, 61)) {
+      if (!wait_warp(BAR(F_S_FULL), j & 1, abort_flag, p.ctl, 61)) {
         ok = false;
         return false;
       }
       tc_fence_after();
       uint32_t v[64];
-      tmem_ld64(tS, v);
+      tmem_ld64(tl + LY::kTmemS + 64 * half, v);
+      // S is in registers: the MMA thread may compute the next tile's S over it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(F_S_READ));
 #pragma unroll
       for (int c = 0; c < 64; ++c) v[c] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2)));
       if (masked) {
@@ -662,19 +676,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
       tc_fence_after();
-      uint32_t dp[64];
-      tmem_ld64(tl + LY::kTmemDP + 64 * half, dp);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(F_DP_FREE));  // dP(j+1) may overwrite it now
+      // dS = P * (dP - D), 32 dP columns at a time, packed (column m: keys 2m, 2m + 1)
+      // over the first 32 of this thread's 64 dP columns once they are read
+      const uint32_t tdp = tl + LY::kTmemDP + 64 * half;
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        v[c] = __float_as_uint(__uint_as_float(v[c]) * (__uint_as_float(dp[c]) - Drow));
-      tmem_st_bf16x64(tS, v);  // dS over columns this thread has read
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t d[32];
+        tmem_ld32(tdp + 32 * hh, d);
+        tmem_ld_wait(d);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = 32 * hh + 2 * u;
+          pk[u] = pack_bf16x2(__uint_as_float(v[c]) * (__uint_as_float(d[2 * u]) - Drow),
+                              __uint_as_float(v[c + 1]) * (__uint_as_float(d[2 * u + 1]) - Drow));
+        }
+        tmem_st16(tdp + 16 * hh, pk);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(F_DS_FULL + (j & 1)));
+      if (lane == 0) mbar_arrive(BAR(F_DS_FULL));
       ++j;
       return true;
     });
