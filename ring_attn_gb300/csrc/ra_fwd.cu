@@ -295,33 +295,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c_lo = 0, c_hi = kTileN;
       if (!kv_tile_full(p, qt, s, kt)) row_key_window(p, gq, rk_lo, rk_hi, s, kt, c_lo, c_hi);
       const bool masked = c_lo > 0 || c_hi < kTileN;
-      // all 128 scores of the row in registers: four loads, one wait
+      // all 128 scores of the row in registers, in two halves: the row max of the
+      // first half runs while the second half is loading
       uint32_t v[kTileN];
       tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
       tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
       tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 0));
       tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 64));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 96));
-      if (masked) {
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      float mc[4];
 #pragma unroll
-        for (int c = 0; c < kTileN; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : __float_as_uint(-INFINITY);
-      }
-      float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
-      float m2 = __uint_as_float(v[2]), m3 = __uint_as_float(v[3]);
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1) {
+          tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 64));
+          tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        }
+        if (masked) {
 #pragma unroll
-      for (int c = 4; c < kTileN; c += 4) {
-        m0 = fmaxf(m0, __uint_as_float(v[c]));
-        m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-        m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-        m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+          for (int c = 64 * hh; c < 64 * hh + 64; ++c)
+            v[c] = (c >= c_lo && c < c_hi) ? v[c] : __float_as_uint(-INFINITY);
+        }
+        // four chains of three-input maxima over the 64 scores of this half
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c0 = 64 * hh + 16 * q;
+          float m = hh == 0 ? __uint_as_float(v[c0]) : fmaxf(mc[q], __uint_as_float(v[c0]));
+#pragma unroll
+          for (int c = c0 + 1; c < c0 + 15; c += 2) m = fmax3f(m, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+          mc[q] = fmaxf(m, __uint_as_float(v[c0 + 15]));
+        }
       }
-      m0 = fmaxf(m0, m2);
-      m1 = fmaxf(m1, m3);
       // raw scores: the scale is > 0, so max(s) * scale = max(s * scale)
-      const float mx = fmaxf(m0, m1) * p.scale_log2;
+      const float mx = fmax3f(mc[0], mc[1], fmaxf(mc[2], mc[3])) * p.scale_log2;
       float alpha = 1.f;
       if (mx > -INFINITY) {
         if (m_run == -INFINITY) {
@@ -335,20 +341,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P = exp2(s * scale - m) and the row sum; P goes as bf16 pairs over the
       // first 64 columns of this tile's S columns (column 16 c32 + u holds keys
       // 32 c32 + 2u and 32 c32 + 2u + 1); the scores are already in registers.
-      float s0 = 0.f, s1 = 0.f;
+      // s * scale - m and the sums run two lanes per instruction (f32x2).
+      const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2), nm2 = f32x2(-m_use, -m_use);
+      uint64_t acc[4] = {0, 0, 0, 0};  // four pairs of partial row sums (+0.0f bits)
 #pragma unroll
       for (int c32 = 0; c32 < kTileN / 32; ++c32) {
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float e0 = fast_exp2(fmaf(__uint_as_float(v[c32 * 32 + 2 * u]), p.scale_log2, -m_use));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(v[c32 * 32 + 2 * u + 1]), p.scale_log2, -m_use));
-          s0 += e0;
-          s1 += e1;
+          const int c = c32 * 32 + 2 * u;
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc2, nm2), x0, x1);
+          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          acc[u & 3] = add_f32x2(acc[u & 3], f32x2(e0, e1));
           pk[u] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + c32 * 16, pk);
       }
+      float s0, s1;
+      f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), s0, s1);
       l_run = l_run * alpha + (s0 + s1);
       // O_t is stable here (the commit behind S_FULL covers PV_t(j-1)) and PV_t(j)
       // waits for P_FULL, so the rescale fits between them
