@@ -140,7 +140,7 @@ ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tens
  * cannot hand over device memory, e.g. an integration point whose signature
  * has no workspace argument, or a process whose device memory is already
  * fully reserved by another allocator, so that allocating at that point would
- * fail.  It allocates nothing: the per-row statistics (D and lse * log2(e))
+ * fail.  It allocates nothing: the per-row statistics (-D and -lse * log2(e))
  * live in one array of RA_STATIC_SCRATCH_BYTES bytes that the library holds
  * in device memory on every device that loads it, until the process exits (a
  * file-scope __device__ array).
@@ -198,7 +198,7 @@ ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, 
                               void* stream);
 
 /* Workspace bytes needed by `op` (ra_op) for (b, h, s, d) split into n_shards
- * shards; 0 for RA_OP_FWD.  RA_OP_BWD: D = rowsum(dO*O) and lse*log2(e) per
+ * shards; 0 for RA_OP_FWD.  RA_OP_BWD: -D = -rowsum(dO*O) and -lse*log2(e) per
  * query row, each laid out per shard with the shard's rows padded to a
  * multiple of 128 (b*h*n_shards*ceil(s/n_shards/128)*128 floats each), each
  * part 256-byte aligned.  Varlen calls use b = 1, s = total.  0 on bad sizes. */

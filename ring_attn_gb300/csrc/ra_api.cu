@@ -240,7 +240,7 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   return cuda_status(launch_fwd((int)q.d, tq, tk, tv, p, static_cast<cudaStream_t>(stream)));
 }
 
-// Workspace: D and lse2, each laid out per shard with rows padded to a
+// Workspace: -D and -lse2, each laid out per shard with rows padded to a
 // multiple of 128, each part 256-byte aligned.
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 long long stat_rows_per_shard(long long s, int n_shards) {
@@ -266,8 +266,8 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, n_shards)) return RA_ERR_WORKSPACE;
   const int stat_L = (int)stat_rows_per_shard(q.s, n_shards);
   const size_t stats = round256((size_t)q.b * q.h * n_shards * stat_L * sizeof(float));
-  float* Dsum = static_cast<float*>(ws);
-  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + stats);
+  float* nD = static_cast<float*>(ws);
+  float* nlse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + stats);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   View4 vdo{dout.data, dout.sb, dout.sh, dout.ss, (int)dout.b, (int)dout.h, (int)dout.s, (int)dout.d};
@@ -287,8 +287,8 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.stat_L = stat_L;
-  p.lse2 = lse2;
-  p.Dsum = Dsum;
+  p.nlse2 = nlse2;
+  p.nD = nD;
   p.dq = dq.data;
   p.dk = dk.data;
   p.dv = dv.data;
@@ -311,7 +311,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, Dsum, lse2, n_shards, stat_L, st)));
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, n_shards, stat_L, st)));
   }
   {
     TimedLaunch tl(RA_KERNEL_BWD, st);
@@ -346,7 +346,7 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
 
 }  // namespace
 
-// Statistics of ring_attn_bwd_static_scratch (D, then lse * log2(e)).  The
+// Statistics of ring_attn_bwd_static_scratch (-D, then -lse * log2(e)).  The
 // library never allocates it: it is part of the loaded device image.  In host
 // code this name is only a stand-in; static_scratch gives the device address.
 static __device__ __align__(256) unsigned char g_bwd_scratch[RA_STATIC_SCRATCH_BYTES];

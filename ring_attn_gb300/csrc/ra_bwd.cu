@@ -68,7 +68,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, bool v
 }
 
 // ======================================================================== dK / dV
-// Warps: 0 TMA (K, V once; Q with the query tile's lse2 / D, and dO, into two
+// Warps: 0 TMA (K, V once; Q with the query tile's -lse2 / -D, and dO, into two
 // 2-stage rings), 1 MMA, 2 TMEM; warpgroups 1 and 2: one key row each, query
 // columns [0, 64) and [64, 128).  TMEM: S^T [0,128), dP^T [128,256), dV
 // [256, 256+D), dK [256+D, 256+2D).  A thread reads its 64 S^T columns into
@@ -87,7 +87,7 @@ struct DkdvLayout {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;          // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;     // 2 stages
-  static constexpr int kStats = kDO + 2 * kTile; // 2 stages (with Q) x (lse2, D), 128 floats each
+  static constexpr int kStats = kDO + 2 * kTile; // 2 stages (with Q) x (-lse2, -D), 128 floats each
   static constexpr int kBar = kStats + 2 * 2 * 512;
   static constexpr int kNumBars = 15;
   static constexpr int kMisc = kBar + kNumBars * 8;
@@ -97,7 +97,7 @@ struct DkdvLayout {
 
 enum DkdvBar {
   E_KV_FULL = 0,
-  E_Q_FULL = 1,     // 2: Q, lse2 and D of a query tile
+  E_Q_FULL = 1,     // 2: Q, -lse2 and -D of a query tile
   E_Q_EMPTY = 3,    // 2
   E_DO_FULL = 5,    // 2
   E_DO_EMPTY = 7,   // 2
@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((i >> 1) - 1) & 1;
         const int qrow = r * p.L + qt * kTileM;
         if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) return false;
-        // lse2 / D of the tile's 128 query rows: 512-byte aligned in the padded layout
+        // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
         const long long e0 = stat_bh + (long long)r * p.stat_L + qt * kTileM;
         mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
-        bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.lse2 + e0, 512, BAR(E_Q_FULL + st));
-        bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.Dsum + e0, 512, BAR(E_Q_FULL + st));
+        bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(E_Q_FULL + st));
+        bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(E_Q_FULL + st));
         if (i >= 2 && !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)) {
           drain_one(BAR(E_Q_FULL + st), (i >> 1) & 1, p.ctl, 43);
           return false;
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int i = 0;
     walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
       const int st = i & 1;
-      // padding query rows have lse2 = +inf and D = 0 (P = 0, dS = 0) without a mask
+      // padding query rows have -lse2 = -inf and -D = 0 (P = 0, dS = 0) without a mask
       int c_lo = 0, c_hi = kTileM;
       if (!q_tile_full<kTileM>(p, k, r, qt)) key_query_window<kTileM>(p, valid_k, gk, rq_lo, rq_hi, r, qt, c_lo, c_hi);
       c_lo -= 64 * half;
@@ -324,13 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(E_S_READ));
+      // P^T = exp2(s * scale - lse2), s * scale - lse2 two lanes per instruction
+      const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l = ls4[c4];
-        v[4 * c4 + 0] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[4 * c4 + 0]), p.scale_log2, -l.x)));
-        v[4 * c4 + 1] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[4 * c4 + 1]), p.scale_log2, -l.y)));
-        v[4 * c4 + 2] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[4 * c4 + 2]), p.scale_log2, -l.z)));
-        v[4 * c4 + 3] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[4 * c4 + 3]), p.scale_log2, -l.w)));
+        float x0, x1, x2, x3;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1])), sc2, f32x2(l.x, l.y)),
+                    x0, x1);
+        f32x2_split(
+            fma_f32x2(f32x2(__uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3])), sc2, f32x2(l.z, l.w)),
+            x2, x3);
+        v[4 * c4 + 0] = __float_as_uint(fast_exp2(x0));
+        v[4 * c4 + 1] = __float_as_uint(fast_exp2(x1));
+        v[4 * c4 + 2] = __float_as_uint(fast_exp2(x2));
+        v[4 * c4 + 3] = __float_as_uint(fast_exp2(x3));
       }
       if (masked) {
 #pragma unroll
@@ -360,10 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p2 = __uint_as_float(v[c + 2]), p3 = __uint_as_float(v[c + 3]);
           pp[2 * c4] = pack_bf16x2(p0, p1);
           pp[2 * c4 + 1] = pack_bf16x2(p2, p3);
-          ps[16 * hh + 2 * c4] = pack_bf16x2(p0 * (__uint_as_float(d[4 * c4]) - dd.x),
-                                             p1 * (__uint_as_float(d[4 * c4 + 1]) - dd.y));
-          ps[16 * hh + 2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(d[4 * c4 + 2]) - dd.z),
-                                                 p3 * (__uint_as_float(d[4 * c4 + 3]) - dd.w));
+          // dS^T = P^T * (dP^T + (-D)), two lanes per instruction
+          float s0, s1, s2, s3;
+          f32x2_split(mul_f32x2(f32x2(p0, p1), add_f32x2(f32x2(__uint_as_float(d[4 * c4]), __uint_as_float(d[4 * c4 + 1])),
+                                                         f32x2(dd.x, dd.y))),
+                      s0, s1);
+          f32x2_split(mul_f32x2(f32x2(p2, p3), add_f32x2(f32x2(__uint_as_float(d[4 * c4 + 2]),
+                                                                __uint_as_float(d[4 * c4 + 3])),
+                                                         f32x2(dd.z, dd.w))),
+                      s2, s3);
+          ps[16 * hh + 2 * c4] = pack_bf16x2(s0, s1);
+          ps[16 * hh + 2 * c4 + 1] = pack_bf16x2(s2, s3);
         }
         tmem_st16(tdp + 16 * hh, pp);
       }
@@ -619,10 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       rk_lo = __ldg(p.cu + sg);
       rk_hi = p.causal ? gq + 1 : __ldg(p.cu + sg + 1);
     }
-    // this row's statistics (padding rows: lse2 = +inf, D = 0, so P = dS = 0)
+    // this row's statistics, negated (padding rows: -lse2 = -inf, -D = 0, so P = dS = 0)
     const long long srow = (((long long)b * p.H + h) * p.N + r) * p.stat_L + i;
-    const float lse2 = __ldg(p.lse2 + srow);
-    const float Drow = __ldg(p.Dsum + srow);
+    const uint64_t nl2 = f32x2(__ldg(p.nlse2 + srow), __ldg(p.nlse2 + srow));
+    const uint64_t nD2 = f32x2(__ldg(p.nD + srow), __ldg(p.nD + srow));
+    const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
     // warpgroup 1 copies the row's Q, warpgroup 2 its dO, into tensor memory as
     // packed bf16 (column m: head-dim elements 2m, 2m + 1) for the S and dP MMAs
     bool ok = n_tiles == 0 || wait_warp(BAR(F_QDO_FULL), 0, abort_flag, p.ctl, 64);
@@ -666,7 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(F_S_READ));
 #pragma unroll
-      for (int c = 0; c < 64; ++c) v[c] = __float_as_uint(fast_exp2(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2)));
+      for (int c = 0; c < 64; c += 2) {
+        // P = exp2(s * scale - lse2), s * scale - lse2 two lanes per instruction
+        float x0, x1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc2, nl2), x0, x1);
+        v[c] = __float_as_uint(fast_exp2(x0));
+        v[c + 1] = __float_as_uint(fast_exp2(x1));
+      }
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : 0u;
@@ -688,8 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int c = 32 * hh + 2 * u;
-          pk[u] = pack_bf16x2(__uint_as_float(v[c]) * (__uint_as_float(d[2 * u]) - Drow),
-                              __uint_as_float(v[c + 1]) * (__uint_as_float(d[2 * u + 1]) - Drow));
+          // dS = P * (dP + (-D)), two lanes per instruction
+          float s0, s1;
+          f32x2_split(mul_f32x2(f32x2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                add_f32x2(f32x2(__uint_as_float(d[2 * u]), __uint_as_float(d[2 * u + 1])), nD2)),
+                      s0, s1);
+          pk[u] = pack_bf16x2(s0, s1);
         }
         tmem_st16(tdp + 16 * hh, pk);
       }

@@ -35,8 +35,8 @@ struct BwdParams {
   int stat_L;               // per-shard rows of the statistics arrays: n_qtiles * 128
   float scale;              // softmax scale
   float scale_log2;
-  const float* lse2;        // lse * log2(e), (b, h, shard, stat_L); padding rows hold +inf
-  const float* Dsum;        // rowsum(dO * O), same layout; padding rows hold 0
+  const float* nlse2;       // -lse * log2(e), (b, h, shard, stat_L); padding rows hold -inf
+  const float* nD;          // -rowsum(dO * O), same layout; padding rows hold 0
   void* dq;                 // bf16 outputs
   void* dk;
   void* dv;
@@ -63,13 +63,14 @@ size_t fwd_smem_bytes(int D);
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st);
 
-// Per query row: D = rowsum(dO * O) and lse2 = lse * log2(e), stored per shard
-// with the rows padded to stat_L (padding rows get D = 0, lse2 = +inf).
+// Per query row: -D = -rowsum(dO * O) and -lse2 = -lse * log2(e), stored per
+// shard with the rows padded to stat_L (padding rows get 0 and -inf); negated so
+// that the backward adds them in packed f32x2 arithmetic.
 struct LseView {
   const float* data;
   long long sb, sh, ss;
 };
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2, int N,
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
                            int stat_L, cudaStream_t st);
 
 struct MergeArgs {

@@ -132,11 +132,11 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
 }
 
 // ------------------------------------------------------------------ backward pre / post
-// Per query row: D = sum_d dO * O and lse2 = lse * log2(e), stored per shard
-// with each shard's rows padded to stat_L (padding: D = 0, lse2 = +inf, so a
+// Per query row: -D = -sum_d dO * O and -lse2 = -lse * log2(e), stored per shard
+// with each shard's rows padded to stat_L (padding: -D = 0, -lse2 = -inf, so a
 // padded column contributes P = 0 and dS = 0).  d/8 threads per row (8 bf16 each).
-__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* Dsum,
-                                                            float* lse2, int N, int stat_L) {
+__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* nD,
+                                                            float* nlse2, int N, int stat_L) {
   const int tpr = dout.d / 8;  // threads per row
   const int L = dout.s / N;
   const long long rows = (long long)dout.b * dout.h * N * stat_L;
@@ -172,8 +172,8 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
     }
     for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && part == 0) {
-      Dsum[row] = acc;
-      lse2[row] = real ? lse.data[b * lse.sb + h * lse.sh + p * lse.ss] * 1.4426950408889634f : INFINITY;
+      nD[row] = -acc;
+      nlse2[row] = real ? lse.data[b * lse.sb + h * lse.sh + p * lse.ss] * -1.4426950408889634f : -INFINITY;
     }
   }
 }
@@ -226,10 +226,10 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* Dsum, float* lse2, int N,
+cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
                            int stat_L, cudaStream_t st) {
   const long long total = (long long)dout.b * dout.h * N * stat_L * (dout.d / 8);
-  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, Dsum, lse2, N, stat_L);
+  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L);
   return cudaGetLastError();
 }
 
