@@ -95,6 +95,14 @@ struct DkdvLayout {
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
 };
 
+// Register split of the dK / dV kernel: the control warpgroup (TMA, MMA, TMEM)
+// gives registers to the two elementwise warpgroups.  The launch allocation is
+// kThreads * kDkdvLaunchRegs; the launcher checks the compiled kernel against it.
+constexpr int kDkdvLaunchRegs = 168;
+constexpr int kDkdvRegsLow = 72;
+constexpr int kDkdvRegsHigh = 216;
+static_assert(128 * kDkdvRegsLow + 256 * kDkdvRegsHigh <= kThreads * kDkdvLaunchRegs, "register split exceeds the launch");
+
 enum DkdvBar {
   E_KV_FULL = 0,
   E_Q_FULL = 1,     // 2: Q, -lse2 and -D of a query tile
@@ -168,7 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const long long stat_bh = ((long long)b * p.H + h) * p.N * p.stat_L;  // statistics row of (b, h, shard 0)
 
-  if (warp == 0) {
+  if (warp < 4) {
+    regs_dec<kDkdvRegsLow>();
+    if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_tiles > 0) {
       int issued[2] = {0, 0};
@@ -285,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_one(BAR(E_TEARDOWN), 0, p.ctl, 42);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+    }
+  } else {
+    regs_inc<kDkdvRegsHigh>();
     // ------------------------------------------------------------ P^T and dS^T, half a key row per thread
     const int half = (warp - 4) >> 2;  // query columns [64 half, 64 half + 64)
     const int jr = ((warp - 4) & 3) * 32 + lane;
@@ -751,8 +763,12 @@ template <int D>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st) {
   if (which == 0) {
-    cudaError_t e = cudaFuncSetAttribute(ring_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DkdvLayout<D>::kAlloc);
+    // the register split inside the kernel is only safe with the launch allocation it was sized for
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, ring_dkdv_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kDkdvLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(ring_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.N * p.n_ktiles), (unsigned)(p.B * p.H));
     ring_dkdv_kernel<D><<<grid, kThreads, DkdvLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, p);
