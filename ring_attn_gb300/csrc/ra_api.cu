@@ -487,8 +487,13 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
     a.la_s2 = f_la;
     a.lb_s2 = f_lb;
   }
+  // 8 columns per thread (two 16-byte fp32 accesses, one 16-byte bf16 access)
+  // when every row start allows it
+  const bool v8 = d % 8 == 0 && 32 % (d / 8) == 0 && oa[0] % 8 == 0 && oa[1] % 8 == 0 && oa[2] % 8 == 0 &&
+                  ob[0] % 8 == 0 && ob[1] % 8 == 0 && ob[2] % 8 == 0 && aligned(out_blk->data, 16);
+  a.vec = v8 ? 8 : 4;
   a.qshift = 0;
-  while ((1LL << a.qshift) < d / 4) ++a.qshift;
+  while ((1LL << a.qshift) < d / a.vec) ++a.qshift;
   TimedLaunch tl(RA_KERNEL_LSE_MERGE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_lse_merge(a, static_cast<cudaStream_t>(stream)));
 }

@@ -49,35 +49,36 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vp
 }
 
 // ------------------------------------------------------------------ LSE merge
-// A group of d/4 threads (d/4 divides 32, so a group sits inside one warp)
-// owns a row, 4 columns per thread:
+// A group of d/VEC threads (a power of two dividing 32, so a group sits inside
+// one warp) owns a row, VEC consecutive columns per thread:
 //   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
 //   out_acc += w * (out_blk - out_acc).
-// Each thread handles kUnroll rows per loop turn and issues every load before
-// using any, so that enough bytes are in flight to keep HBM busy.  Loop
-// control is warp-uniform: every lane of a row has read the old lse_acc
-// (before __syncwarp) before the row's first lane overwrites it.
-constexpr int kUnroll = 2;
-
-template <bool BLK_F32>
+// Each thread handles UNROLL rows per loop turn and issues every load before
+// using any, so that enough bytes are in flight to keep HBM busy; the row data
+// is read and written once, with streaming cache hints.  Loop control is
+// warp-uniform: every lane of a row has read the old lse_acc (before
+// __syncwarp) before the row's first lane overwrites it.
+template <bool BLK_F32, int VEC, int UNROLL>
 __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
-  const long long q_per_row = a.d / 4;
-  const long long total = a.rows * q_per_row;
+  constexpr int NV = VEC / 4;  // float4 of out_acc per thread
+  const long long per_row = a.d / VEC;
+  const long long total = a.rows * per_row;
   const long long step = (long long)gridDim.x * blockDim.x;
   const int lane = threadIdx.x & 31;
   for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x - lane; base < total;
-       base += kUnroll * step) {
-    float* oa[kUnroll];
-    float* la[kUnroll];
-    float A[kUnroll], B[kUnroll];
-    float4 ob[kUnroll], oc[kUnroll];
-    bool live[kUnroll];
-    long long c4[kUnroll];
+       base += UNROLL * step) {
+    float* oa[UNROLL];
+    float* la[UNROLL];
+    float A[UNROLL], B[UNROLL];
+    float4 ob[UNROLL][NV], oc[UNROLL][NV];
+    bool live[UNROLL];
+    bool first[UNROLL];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const long long t = base + u * step + lane;
       live[u] = t < total;
-      c4[u] = live[u] ? (t & (q_per_row - 1)) : 0;  // d / 4 is a power of two
+      const long long c = live[u] ? (t & (per_row - 1)) : 0;  // per_row is a power of two
+      first[u] = c == 0;
       long long rw = live[u] ? (t >> a.qshift) : 0;
       long long i0 = 0, i1 = 0, i2 = rw;
       if (!a.flat) {
@@ -86,47 +87,63 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
         i1 = rw % a.n1;
         i0 = rw / a.n1;
       }
-      oa[u] = a.out_acc + i0 * a.oa_s0 + i1 * a.oa_s1 + i2 * a.oa_s2 + 4 * c4[u];
+      oa[u] = a.out_acc + i0 * a.oa_s0 + i1 * a.oa_s1 + i2 * a.oa_s2 + VEC * c;
       la[u] = a.lse_acc + i0 * a.la_s0 + i1 * a.la_s1 + i2 * a.la_s2;
       const float* lb = a.lse_blk + i0 * a.lb_s0 + i1 * a.lb_s1 + i2 * a.lb_s2;
-      const long long bofs = i0 * a.ob_s0 + i1 * a.ob_s1 + i2 * a.ob_s2 + 4 * c4[u];
+      const long long bofs = i0 * a.ob_s0 + i1 * a.ob_s1 + i2 * a.ob_s2 + VEC * c;
       A[u] = live[u] ? *la[u] : 0.f;
       B[u] = live[u] ? __ldg(lb) : -INFINITY;
-      oc[u] = live[u] ? *reinterpret_cast<const float4*>(oa[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        oc[u][k] = live[u] ? __ldcs(reinterpret_cast<const float4*>(oa[u]) + k) : make_float4(0.f, 0.f, 0.f, 0.f);
       if (BLK_F32) {
-        ob[u] = live[u] ? __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          ob[u][k] = live[u] ? __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs) + k)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else if (VEC == 8) {
+        const uint4 raw = live[u] ? __ldcs(reinterpret_cast<const uint4*>(
+                                        reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        ob[u][0] = make_float4(__low2float(h[0]), __high2float(h[0]), __low2float(h[1]), __high2float(h[1]));
+        ob[u][NV - 1] = make_float4(__low2float(h[2]), __high2float(h[2]), __low2float(h[3]), __high2float(h[3]));
       } else {
-        const uint2 raw = live[u] ? __ldg(reinterpret_cast<const uint2*>(
+        const uint2 raw = live[u] ? __ldcs(reinterpret_cast<const uint2*>(
                                         reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs))
                                   : make_uint2(0u, 0u);
         const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
         const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        ob[u] = make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+        ob[u][0] = make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
       }
     }
     __syncwarp();
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       if (!live[u]) continue;
-      float4 r;
+      float4 r[NV];
       float lse_new;
       if (B[u] == -INFINITY) {
         // empty block: unchanged, except that an empty accumulator is normalised to out = 0
         if (A[u] != -INFINITY) continue;
-        r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) r[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         lse_new = -INFINITY;
       } else if (A[u] == -INFINITY) {
-        r = ob[u];  // empty accumulator: take the block
+#pragma unroll
+        for (int k = 0; k < NV; ++k) r[k] = ob[u][k];  // empty accumulator: take the block
         lse_new = B[u];
       } else {
         lse_new = fmaxf(A[u], B[u]) + log1pf(expf(-fabsf(A[u] - B[u])));
         const float w = expf(B[u] - lse_new);
-        r = make_float4(oc[u].x + w * (ob[u].x - oc[u].x), oc[u].y + w * (ob[u].y - oc[u].y),
-                        oc[u].z + w * (ob[u].z - oc[u].z), oc[u].w + w * (ob[u].w - oc[u].w));
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          r[k] = make_float4(oc[u][k].x + w * (ob[u][k].x - oc[u][k].x), oc[u][k].y + w * (ob[u][k].y - oc[u][k].y),
+                             oc[u][k].z + w * (ob[u][k].z - oc[u][k].z), oc[u][k].w + w * (ob[u][k].w - oc[u][k].w));
       }
-      *reinterpret_cast<float4*>(oa[u]) = r;
-      if (c4[u] == 0) *la[u] = lse_new;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) __stcs(reinterpret_cast<float4*>(oa[u]) + k, r[k]);
+      if (first[u]) *la[u] = lse_new;
     }
   }
 }
@@ -219,10 +236,17 @@ cudaError_t launch_permute(const PermuteArgs& a_in, cudaStream_t st) {
 
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
   const long long total = a.rows * (a.d / 4);
-  if (a.blk_f32)
-    lse_merge_kernel<true><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
-  else
-    lse_merge_kernel<false><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
+  if (a.vec == 8) {
+    const long long items = a.rows * (a.d / 8);
+    if (a.blk_f32)
+      lse_merge_kernel<true, 8, 2><<<grid_for(items, kThreads), kThreads, 0, st>>>(a);
+    else
+      lse_merge_kernel<false, 8, 4><<<grid_for(items, kThreads), kThreads, 0, st>>>(a);
+  } else if (a.blk_f32) {
+    lse_merge_kernel<true, 4, 2><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
+  } else {
+    lse_merge_kernel<false, 4, 2><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

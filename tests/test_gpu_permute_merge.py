@@ -75,7 +75,8 @@ def _merge_case(rows_shape, d, blk_dtype, seed):
 
 
 @pytest.mark.parametrize("blk_dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("shape,d", [((2, 3, 200), 128), ((7, 129), 64), ((2, 4, 50), 128), ((33,), 16)])
+@pytest.mark.parametrize("shape,d", [((2, 3, 200), 128), ((7, 129), 64), ((2, 4, 50), 128), ((33,), 16),
+                                     ((9, 31), 4)])
 def test_lse_merge_matches_oracle(ra, blk_dtype, shape, d):
     oa, la, ob, lb = _merge_case(shape, d, blk_dtype, 3)
     ref_o, ref_l = oracle.lse_merge(oa.numpy().reshape(-1, d), la.numpy().reshape(-1),
@@ -87,9 +88,10 @@ def test_lse_merge_matches_oracle(ra, blk_dtype, shape, d):
     assert_lse_close("lse_acc", gla.cpu().reshape(-1), ref_l, tol=1e-5)
 
 
-def test_lse_merge_strided_views(ra):
+@pytest.mark.parametrize("width", [256, 132])  # 132: rows 16-byte but not 32-byte aligned (4 columns per thread)
+def test_lse_merge_strided_views(ra, width):
     g = torch.Generator("cpu").manual_seed(4)
-    big_o = torch.randn(3, 40, 256, generator=g)
+    big_o = torch.randn(3, 40, width, generator=g)
     big_l = torch.randn(3, 80, generator=g)
     oa, la = big_o[:, :, :128], big_l[:, ::2]
     ob = torch.randn(3, 40, 128, generator=g).to(torch.bfloat16)
