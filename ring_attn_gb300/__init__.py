@@ -19,7 +19,9 @@ __all__ = [
     "ring_attn_varlen_fwd", "ring_attn_varlen_bwd", "lse_merge", "ring_attn_permute", "ring_attn_unpermute",
     "ring_attn_workspace_size", "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_version",
     "ring_attn_timing_enable", "ring_attn_timing_read", "ring_attn_bwd_static_scratch", "EXPORTED_SYMBOLS",
-    "KERNELS", "RA_STATIC_SCRATCH_BYTES",
+    "KERNELS", "RA_STATIC_SCRATCH_BYTES", "ring_attn_qkvpacked_fwd", "ring_attn_qkvpacked_bwd", "ring_attn_kvpacked_fwd",
+    "ring_attn_kvpacked_bwd", "ring_attn_varlen_qkvpacked_fwd", "ring_attn_varlen_qkvpacked_bwd",
+    "ring_attn_varlen_kvpacked_fwd", "ring_attn_varlen_kvpacked_bwd",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -285,6 +287,104 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "ring_attn_varlen_bwd")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------- packed forms
+# The "kvpacked" / "qkvpacked" entry points of the "Ring Flash Attention" README
+# (API list) take k and v, or q, k and v, stacked in one tensor.  They are
+# strided views over the calls above: the kernels read the packed tensors in
+# place through their strides, and the gradients are written into one packed
+# tensor the same way.  Batched forms use the flash-attention packing
+# (b, s, 3 or 2, h, d) with out and dout as (b, s, h, d); varlen forms use
+# (total, 3 or 2, h, d) with out and dout as (total, h, d).  The sequence axis
+# is in layout order, as everywhere in this library.
+
+def _bshd(x):
+    """(b, s, h, d) -> the (b, h, s, d) view the calls take."""
+    return x.transpose(1, 2)
+
+
+def ring_attn_qkvpacked_fwd(qkv, layout="contiguous", n_shards=1, causal=False, softmax_scale=None, out=None,
+                            lse=None, stream=None):
+    """qkv: (b, s, 3, h, d) bf16.  Returns (out (b, s, h, d) bf16, lse (b, h, s) fp32)."""
+    b, s, three, h, d = qkv.shape
+    if three != 3:
+        raise ValueError("qkv must be (b, s, 3, h, d)")
+    out = torch.empty((b, s, h, d), dtype=qkv.dtype, device=qkv.device) if out is None else out
+    _, lse = ring_attn_fwd(_bshd(qkv[:, :, 0]), _bshd(qkv[:, :, 1]), _bshd(qkv[:, :, 2]), layout, n_shards, causal,
+                           softmax_scale, out=_bshd(out), lse=lse, stream=stream)
+    return out, lse
+
+
+def ring_attn_qkvpacked_bwd(dout, qkv, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
+                            dqkv=None, workspace=None, stream=None):
+    """Gradient of ring_attn_qkvpacked_fwd: dqkv (b, s, 3, h, d) bf16."""
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    ring_attn_bwd(_bshd(dout), _bshd(qkv[:, :, 0]), _bshd(qkv[:, :, 1]), _bshd(qkv[:, :, 2]), _bshd(out), lse,
+                  layout, n_shards, causal, softmax_scale, dq=_bshd(dqkv[:, :, 0]), dk=_bshd(dqkv[:, :, 1]),
+                  dv=_bshd(dqkv[:, :, 2]), workspace=workspace, stream=stream)
+    return dqkv
+
+
+def ring_attn_kvpacked_fwd(q, kv, layout="contiguous", n_shards=1, causal=False, softmax_scale=None, out=None,
+                           lse=None, stream=None):
+    """q: (b, s, h, d), kv: (b, s, 2, h, d) bf16.  Returns (out (b, s, h, d), lse (b, h, s))."""
+    if kv.dim() != 5 or kv.shape[2] != 2:
+        raise ValueError("kv must be (b, s, 2, h, d)")
+    out = torch.empty_like(q) if out is None else out
+    _, lse = ring_attn_fwd(_bshd(q), _bshd(kv[:, :, 0]), _bshd(kv[:, :, 1]), layout, n_shards, causal,
+                           softmax_scale, out=_bshd(out), lse=lse, stream=stream)
+    return out, lse
+
+
+def ring_attn_kvpacked_bwd(dout, q, kv, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
+                           dq=None, dkv=None, workspace=None, stream=None):
+    """Gradient of ring_attn_kvpacked_fwd: (dq (b, s, h, d), dkv (b, s, 2, h, d))."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dkv = torch.empty_like(kv) if dkv is None else dkv
+    ring_attn_bwd(_bshd(dout), _bshd(q), _bshd(kv[:, :, 0]), _bshd(kv[:, :, 1]), _bshd(out), lse, layout, n_shards,
+                  causal, softmax_scale, dq=_bshd(dq), dk=_bshd(dkv[:, :, 0]), dv=_bshd(dkv[:, :, 1]),
+                  workspace=workspace, stream=stream)
+    return dq, dkv
+
+
+def ring_attn_varlen_qkvpacked_fwd(qkv, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
+                                   out=None, lse=None, stream=None):
+    """qkv: (total, 3, h, d) bf16.  Returns (out (total, h, d), lse (h, total))."""
+    if qkv.dim() != 4 or qkv.shape[1] != 3:
+        raise ValueError("qkv must be (total, 3, h, d)")
+    out = torch.empty_like(qkv[:, 0]) if out is None else out
+    return ring_attn_varlen_fwd(qkv[:, 0], qkv[:, 1], qkv[:, 2], cu_seqlens, max_seqlen, n_shards, causal,
+                                softmax_scale, out=out, lse=lse, stream=stream)
+
+
+def ring_attn_varlen_qkvpacked_bwd(dout, qkv, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
+                                   softmax_scale=None, dqkv=None, workspace=None, stream=None):
+    """Gradient of ring_attn_varlen_qkvpacked_fwd: dqkv (total, 3, h, d)."""
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    ring_attn_varlen_bwd(dout, qkv[:, 0], qkv[:, 1], qkv[:, 2], out, lse, cu_seqlens, max_seqlen, n_shards, causal,
+                         softmax_scale, dq=dqkv[:, 0], dk=dqkv[:, 1], dv=dqkv[:, 2], workspace=workspace,
+                         stream=stream)
+    return dqkv
+
+
+def ring_attn_varlen_kvpacked_fwd(q, kv, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
+                                  out=None, lse=None, stream=None):
+    """q: (total, h, d), kv: (total, 2, h, d).  Returns (out (total, h, d), lse (h, total))."""
+    if kv.dim() != 4 or kv.shape[1] != 2:
+        raise ValueError("kv must be (total, 2, h, d)")
+    return ring_attn_varlen_fwd(q, kv[:, 0], kv[:, 1], cu_seqlens, max_seqlen, n_shards, causal, softmax_scale,
+                                out=out, lse=lse, stream=stream)
+
+
+def ring_attn_varlen_kvpacked_bwd(dout, q, kv, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
+                                  softmax_scale=None, dq=None, dkv=None, workspace=None, stream=None):
+    """Gradient of ring_attn_varlen_kvpacked_fwd: (dq (total, h, d), dkv (total, 2, h, d))."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dkv = torch.empty_like(kv) if dkv is None else dkv
+    ring_attn_varlen_bwd(dout, q, kv[:, 0], kv[:, 1], out, lse, cu_seqlens, max_seqlen, n_shards, causal,
+                         softmax_scale, dq=dq, dk=dkv[:, 0], dv=dkv[:, 1], workspace=workspace, stream=stream)
+    return dq, dkv
 
 
 def ring_attn_permute(x, layout, n_shards, seq_dim=2, out=None, stream=None):
