@@ -23,4 +23,5 @@ from .attention import (  # noqa: F401
     segment_ids,
     token_of_position,
     unpermute,
+    varlen_token_of_position,
 )

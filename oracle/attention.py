@@ -66,17 +66,61 @@ def token_of_position(layout: str, n_shards: int, s: int) -> np.ndarray:
     return g
 
 
-def permute(x, layout: str, n_shards: int, axis: int = -2):
+def varlen_token_of_position(layout: str, n_shards: int, cu_seqlens) -> np.ndarray:
+    """g[p] for one packed buffer of total = cu[-1] tokens split into N shards.
+
+      contiguous: shards are contiguous slices of the packed buffer (total / N
+                  tokens each; sequences may straddle shards): g[p] = p
+                  ([README] API list, "the varlen versions only support passing
+                  one cu_seqlens").
+      zigzag:     the zigzag split applied to every sequence: sequence k
+                  (L_k = cu[k+1] - cu[k] tokens, a multiple of 2N) is cut into
+                  2N chunks of c_k = L_k / (2N); shard r holds, for k = 0, 1, ...
+                  in turn, chunk r then chunk 2N-1-r of sequence k
+                  ([README] API list, zigzag_ring_flash_attn_varlen_func;
+                  [GUIJIA] "Zigzag Ring Attention").
+    """
+    N = int(n_shards)
+    cu = [int(c) for c in cu_seqlens]
+    total = cu[-1]
+    if N < 1 or total % N:
+        raise ValueError("the packed length must be a multiple of n_shards")
+    if layout == "contiguous":
+        return np.arange(total, dtype=np.int64)
+    if layout != "zigzag":
+        raise ValueError(f"varlen supports the contiguous and zigzag layouts, not {layout!r}")
+    lens = [cu[k + 1] - cu[k] for k in range(len(cu) - 1)]
+    if any(n % (2 * N) for n in lens):
+        raise ValueError("zigzag varlen needs every sequence length to be a multiple of 2*n_shards")
+    g = []
+    for r in range(N):
+        for k, n in enumerate(lens):
+            c = n // (2 * N)
+            g.extend(cu[k] + r * c + o for o in range(c))
+            g.extend(cu[k] + (2 * N - 1 - r) * c + o for o in range(c))
+    return np.asarray(g, dtype=np.int64)
+
+
+def _positions(layout, n_shards, s, cu_seqlens):
+    if cu_seqlens is None:
+        return token_of_position(layout, n_shards, s)
+    g = varlen_token_of_position(layout, n_shards, cu_seqlens)
+    if len(g) != s:
+        raise ValueError("cu_seqlens does not cover the sequence axis")
+    return g
+
+
+def permute(x, layout: str, n_shards: int, axis: int = -2, cu_seqlens=None):
     """Original order -> layout order: y[..., p, :] = x[..., g[p], :]."""
     x = np.asarray(x)
-    g = token_of_position(layout, n_shards, x.shape[axis])
+    g = _positions(layout, n_shards, x.shape[axis], cu_seqlens)
     return np.take(x, g, axis=axis)
 
 
-def unpermute(y, layout: str, n_shards: int, axis: int = -2):
+def unpermute(y, layout: str, n_shards: int, axis: int = -2, cu_seqlens=None):
     """Layout order -> original order: x[..., g[p], :] = y[..., p, :]."""
     y = np.asarray(y)
-    g = token_of_position(layout, n_shards, y.shape[axis])
+    g = _positions(layout, n_shards, y.shape[axis], cu_seqlens)
     x = np.empty_like(y)
     idx = [slice(None)] * y.ndim
     idx[axis] = g
@@ -295,16 +339,16 @@ def ring_attention_sharded(q, k, v, layout, n_shards, scale, causal, cu_seqlens=
     Rank r holds shard r of the layout.  At ring step t = 0..N-1 it holds the
     K/V shard (r - t) mod N ([GUIJIA] "详细流程"), computes the block result
     of its Q shard against it, and merges it into its running (out, lse)
-    with ``lse_merge``.  Varlen uses the contiguous layout and one global
-    cu_seqlens over the packed buffer.
+    with ``lse_merge``.  Varlen takes one global cu_seqlens over the packed
+    buffer and the contiguous or zigzag layout (``varlen_token_of_position``).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     b, h, s, d = q.shape
     N = int(n_shards)
     L = s // N
-    g = token_of_position(layout, N, s)
+    g = _positions(layout, N, s, cu_seqlens)
     seg = segment_ids(cu_seqlens, s) if cu_seqlens is not None else None
-    qs, ks, vs = (permute(x, layout, N, axis=2) for x in (q, k, v))
+    qs, ks, vs = (permute(x, layout, N, axis=2, cu_seqlens=cu_seqlens) for x in (q, k, v))
     out_l = np.zeros((b, h, s, d))
     lse_l = np.full((b, h, s), -np.inf)
     for bi in range(b):
@@ -323,7 +367,8 @@ def ring_attention_sharded(q, k, v, layout, n_shards, scale, causal, cu_seqlens=
                     o_acc, l_acc = lse_merge(o_acc, l_acc, ob, lb)
                 out_l[bi, hi, rq] = o_acc
                 lse_l[bi, hi, rq] = l_acc
-    return unpermute(out_l, layout, N, axis=2), unpermute(lse_l[..., None], layout, N, axis=2)[..., 0]
+    return (unpermute(out_l, layout, N, axis=2, cu_seqlens=cu_seqlens),
+            unpermute(lse_l[..., None], layout, N, axis=2, cu_seqlens=cu_seqlens)[..., 0])
 
 
 def online_softmax_attention(q, k, v, scale, causal, kv_block=64, cu_seqlens=None):

@@ -351,9 +351,72 @@ def _pins_hold():
             g = oracle.token_of_position(layout, nn, s)[r * (s // nn):(r + 1) * (s // nn)]
             if list(g[:len(vals)] if prefix else g) != vals:
                 return False
+        if not _varlen_zigzag_pins_hold():
+            return False
         return True
     except (AssertionError, ValueError, IndexError, FloatingPointError):
         return False
+
+
+# Zigzag varlen: the zigzag split applied to every packed sequence.  Worked by
+# hand from that definition for cu_seqlens = [0, 4, 12], N = 2: sequence 0 has
+# chunks {0}, {1}, {2}, {3} and sequence 1 chunks {4,5}, {6,7}, {8,9}, {10,11};
+# shard 0 takes chunks 0 and 3 of each, shard 1 chunks 1 and 2.
+_VZ_EXAMPLE = ([0, 4, 12], 2, [0, 3, 4, 5, 10, 11, 1, 2, 6, 7, 8, 9])
+
+
+def _varlen_zigzag_pins_hold():
+    cu, n, want = _VZ_EXAMPLE
+    if list(oracle.varlen_token_of_position("zigzag", n, cu)) != want:
+        return False
+    for n in (1, 2, 3, 4):  # one sequence: the batched zigzag map
+        if not np.array_equal(oracle.varlen_token_of_position("zigzag", n, [0, 48]),
+                              oracle.token_of_position("zigzag", n, 48)):
+            return False
+    return True
+
+
+def test_varlen_zigzag_layout_pins():
+    assert _varlen_zigzag_pins_hold()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_varlen_zigzag_layout_structure(n):
+    lens = [2 * n * m for m in (3, 1, 0, 5, 2)]
+    cu = cu_seqlens(lens)
+    g = oracle.varlen_token_of_position("zigzag", n, cu)
+    total = cu[-1]
+    assert sorted(g.tolist()) == list(range(total))  # a bijection
+    L = total // n
+    seg = oracle.segment_ids(cu, total)
+    for r in range(n):
+        loc = g[r * L:(r + 1) * L]
+        assert np.all(np.diff(loc) > 0)  # increasing inside every shard
+        for k in range(len(lens)):       # sequence k at local [cu[k]/N, cu[k+1]/N) of every shard
+            assert np.all(seg[loc[cu[k] // n:cu[k + 1] // n]] == k)
+    x = np.random.default_rng(3).standard_normal((2, total, 3))
+    y = oracle.permute(x, "zigzag", n, axis=1, cu_seqlens=cu)
+    assert np.array_equal(oracle.unpermute(y, "zigzag", n, axis=1, cu_seqlens=cu), x)
+    assert np.array_equal(oracle.varlen_token_of_position("contiguous", n, cu), np.arange(total))
+
+
+def test_varlen_zigzag_rejects_bad_sizes():
+    with pytest.raises(ValueError):
+        oracle.varlen_token_of_position("zigzag", 2, [0, 6])      # 6 is not a multiple of 4
+    with pytest.raises(ValueError):
+        oracle.varlen_token_of_position("stripe", 2, [0, 8])
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_zigzag_sharded_then_merged_equals_full(n, causal):
+    lens = [2 * n * m for m in (2, 1, 4)]
+    cu = cu_seqlens(lens)
+    x = _inputs(1, 2, cu[-1], 8, 91 + n, with_do=False)
+    ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], 0.5, causal, cu_seqlens=cu)
+    o, l = oracle.ring_attention_sharded(x["q"], x["k"], x["v"], "zigzag", n, 0.5, causal, cu_seqlens=cu)
+    assert np.allclose(o, ref_o, atol=1e-12, rtol=0)
+    assert np.allclose(l, ref_l, atol=1e-12, rtol=0)
 
 
 def test_pins_hold_on_the_unmodified_oracle():
@@ -405,7 +468,22 @@ def _mutant_layout_stripe(layout, n_shards, s):
     return g
 
 
+def _mutant_varlen_zigzag_order(layout, n_shards, cu_seqlens):
+    g = _ORIG_VTOKEN(layout, n_shards, cu_seqlens)
+    if layout == "zigzag":  # chunk 2N-1-r placed before chunk r in every sequence
+        cu = list(cu_seqlens)
+        out = []
+        for r in range(n_shards):
+            for k in range(len(cu) - 1):
+                c = (cu[k + 1] - cu[k]) // (2 * n_shards)
+                out += [cu[k] + (2 * n_shards - 1 - r) * c + o for o in range(c)]
+                out += [cu[k] + r * c + o for o in range(c)]
+        g = np.asarray(out, dtype=np.int64)
+    return g
+
+
 _ORIG_BLOCK = A.block_attention
+_ORIG_VTOKEN = A.varlen_token_of_position
 _ORIG_MERGE = A.lse_merge
 _ORIG_TOKEN = A.token_of_position
 
@@ -418,6 +496,7 @@ _ORIG_TOKEN = A.token_of_position
     ("lse_merge", _mutant_merge_swapped),
     ("token_of_position", _mutant_layout_zigzag),
     ("token_of_position", _mutant_layout_stripe),
+    ("varlen_token_of_position", _mutant_varlen_zigzag_order),
 ], ids=lambda x: getattr(x, "__name__", x))
 def test_planted_mistake_fails_a_pin(monkeypatch, target, mutant):
     monkeypatch.setattr(A, target, mutant)
