@@ -172,18 +172,26 @@ ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q
  * (h, total) fp32.  cu_seqlens_dev / cu_seqlens_host: the same int32 array of
  * n_seqs + 1 prefix sums (0 = cu[0] <= cu[1] <= ... <= cu[n_seqs] = total);
  * the host copy is validated before launch, the device copy is read by the
- * kernels.  Shards are contiguous slices of the packed buffer (total / N
- * tokens each); attention is confined to each sequence.  Only the contiguous
- * layout is supported. */
+ * kernels.  Attention is confined to each sequence.  Tensors are in layout
+ * order (ring_attn_varlen_permute):
+ *   RA_LAYOUT_CONTIGUOUS: shards are contiguous slices of the packed buffer
+ *     (total / N tokens each; sequences may straddle shards);
+ *   RA_LAYOUT_ZIGZAG: the zigzag split of every sequence ([README] API list,
+ *     zigzag_ring_flash_attn_varlen_func): sequence k, whose length must be a
+ *     multiple of 2N, is cut into 2N chunks and shard r holds chunk r then
+ *     chunk 2N-1-r of each sequence in turn, so sequence k occupies positions
+ *     [cu[k]/N, cu[k+1]/N) of every shard.
+ * Other layouts return RA_ERR_UNSUPPORTED; a zigzag length that is not a
+ * multiple of 2N returns RA_ERR_INVALID_ARG. */
 ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                                const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
-                               int32_t max_seqlen, int32_t n_shards, int32_t causal, float softmax_scale,
-                               ra_tensor* out, ra_tensor* lse, void* workspace, size_t workspace_bytes,
-                               void* stream);
+                               int32_t max_seqlen, int32_t layout, int32_t n_shards, int32_t causal,
+                               float softmax_scale, ra_tensor* out, ra_tensor* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                                const ra_tensor* out, const ra_tensor* lse, const int32_t* cu_seqlens_dev,
-                               const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen,
+                               const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen, int32_t layout,
                                int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk,
                                ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -196,6 +204,17 @@ ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, in
                             void* stream);
 ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,
                               void* stream);
+
+/* Varlen forms of the two above for one packed buffer of total tokens
+ * (cu_seqlens as in the varlen calls; x.shape[seq_dim] == total):
+ * RA_LAYOUT_CONTIGUOUS is the identity (a copy), RA_LAYOUT_ZIGZAG the
+ * per-sequence zigzag split described above the varlen calls. */
+ra_status ring_attn_varlen_permute(const ra_tensor* x, ra_tensor* y, const int32_t* cu_seqlens_dev,
+                                   const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
+                                   int32_t seq_dim, void* stream);
+ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int32_t* cu_seqlens_dev,
+                                     const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
+                                     int32_t seq_dim, void* stream);
 
 /* Workspace bytes needed by `op` (ra_op) for (b, h, s, d) split into n_shards
  * shards; 0 for RA_OP_FWD.  RA_OP_BWD: -D = -rowsum(dO*O) and -lse*log2(e) per

@@ -21,7 +21,8 @@ __all__ = [
     "ring_attn_timing_enable", "ring_attn_timing_read", "ring_attn_bwd_static_scratch", "EXPORTED_SYMBOLS",
     "KERNELS", "RA_STATIC_SCRATCH_BYTES", "ring_attn_qkvpacked_fwd", "ring_attn_qkvpacked_bwd", "ring_attn_kvpacked_fwd",
     "ring_attn_kvpacked_bwd", "ring_attn_varlen_qkvpacked_fwd", "ring_attn_varlen_qkvpacked_bwd",
-    "ring_attn_varlen_kvpacked_fwd", "ring_attn_varlen_kvpacked_bwd",
+    "ring_attn_varlen_kvpacked_fwd", "ring_attn_varlen_kvpacked_bwd", "ring_attn_varlen_permute",
+    "ring_attn_varlen_unpermute",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -34,7 +35,8 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_step", "lse_merge", "ring_attn_bwd", "ring_attn_varlen_fwd",
     "ring_attn_varlen_bwd", "ring_attn_permute", "ring_attn_unpermute", "ring_attn_workspace_size",
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
-    "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch",
+    "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch", "ring_attn_varlen_permute",
+    "ring_attn_varlen_unpermute",
 )
 RA_STATIC_SCRATCH_BYTES = 16 << 20
 KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
@@ -76,8 +78,10 @@ def load():
         "lse_merge": [T, T, T, T, P],
         "ring_attn_bwd": [T, T, T, T, T, T, I32, I32, I32, F32, T, T, T, P, SZ, P],
         "ring_attn_bwd_static_scratch": [T, T, T, T, T, T, I32, I32, I32, F32, T, T, T, P],
-        "ring_attn_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, F32, T, T, P, SZ, P],
-        "ring_attn_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
+        "ring_attn_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, P, SZ, P],
+        "ring_attn_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
+        "ring_attn_varlen_permute": [T, T, P, P, I32, I32, I32, I32, P],
+        "ring_attn_varlen_unpermute": [T, T, P, P, I32, I32, I32, I32, P],
         "ring_attn_permute": [T, T, I32, I32, I32, P],
         "ring_attn_unpermute": [T, T, I32, I32, I32, P],
         "ring_attn_check_device_error": [P, ctypes.POINTER(I32)],
@@ -239,8 +243,9 @@ def _cu_pair(cu_seqlens, device):
 
 
 def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
-                         out=None, lse=None, stream=None):
-    """Packed sequences, one cu_seqlens.  q, k, v: (total, h, d) or (h, total, d) bf16.
+                         out=None, lse=None, stream=None, layout="contiguous"):
+    """Packed sequences, one cu_seqlens.  q, k, v: (total, h, d) or (h, total, d) bf16 in
+    layout order ("contiguous" slices of the packed buffer, or "zigzag" per sequence).
 
     Returns (out like q, lse (h, total) fp32)."""
     lib = load()
@@ -256,14 +261,16 @@ def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causa
     tq, tk, tv, to, tl = _t(q), _t(k), _t(v), _t(out), _t(lse)
     _check(lib.ring_attn_varlen_fwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()), n,
-                                    int(max_seqlen), int(n_shards), int(bool(causal)), _scale(softmax_scale, d),
-                                    ctypes.byref(to), ctypes.byref(tl), None, 0, _stream(stream)),
+                                    int(max_seqlen), _layout(layout), int(n_shards), int(bool(causal)),
+                                    _scale(softmax_scale, d), ctypes.byref(to), ctypes.byref(tl), None, 0,
+                                    _stream(stream)),
            "ring_attn_varlen_fwd")
     return out, lse
 
 
 def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
-                         softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+                         softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None,
+                         layout="contiguous"):
     lib = load()
     host, dev = _cu_pair(cu_seqlens, q.device)
     n = host.numel() - 1
@@ -281,8 +288,8 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
     ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
     r = [ctypes.byref(x) for x in ts]
     _check(lib.ring_attn_varlen_bwd(r[0], r[1], r[2], r[3], r[4], r[5], ctypes.c_void_p(dev.data_ptr()),
-                                    ctypes.c_void_p(host.data_ptr()), n, int(max_seqlen), int(n_shards),
-                                    int(bool(causal)), _scale(softmax_scale, d), r[6], r[7], r[8],
+                                    ctypes.c_void_p(host.data_ptr()), n, int(max_seqlen), _layout(layout),
+                                    int(n_shards), int(bool(causal)), _scale(softmax_scale, d), r[6], r[7], r[8],
                                     ctypes.c_void_p(workspace.data_ptr()),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "ring_attn_varlen_bwd")
@@ -349,42 +356,68 @@ def ring_attn_kvpacked_bwd(dout, q, kv, out, lse, layout="contiguous", n_shards=
 
 
 def ring_attn_varlen_qkvpacked_fwd(qkv, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
-                                   out=None, lse=None, stream=None):
+                                   out=None, lse=None, stream=None, layout="contiguous"):
     """qkv: (total, 3, h, d) bf16.  Returns (out (total, h, d), lse (h, total))."""
     if qkv.dim() != 4 or qkv.shape[1] != 3:
         raise ValueError("qkv must be (total, 3, h, d)")
     out = torch.empty_like(qkv[:, 0]) if out is None else out
     return ring_attn_varlen_fwd(qkv[:, 0], qkv[:, 1], qkv[:, 2], cu_seqlens, max_seqlen, n_shards, causal,
-                                softmax_scale, out=out, lse=lse, stream=stream)
+                                softmax_scale, out=out, lse=lse, stream=stream, layout=layout)
 
 
 def ring_attn_varlen_qkvpacked_bwd(dout, qkv, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
-                                   softmax_scale=None, dqkv=None, workspace=None, stream=None):
+                                   softmax_scale=None, dqkv=None, workspace=None, stream=None, layout="contiguous"):
     """Gradient of ring_attn_varlen_qkvpacked_fwd: dqkv (total, 3, h, d)."""
     dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
     ring_attn_varlen_bwd(dout, qkv[:, 0], qkv[:, 1], qkv[:, 2], out, lse, cu_seqlens, max_seqlen, n_shards, causal,
                          softmax_scale, dq=dqkv[:, 0], dk=dqkv[:, 1], dv=dqkv[:, 2], workspace=workspace,
-                         stream=stream)
+                         stream=stream, layout=layout)
     return dqkv
 
 
 def ring_attn_varlen_kvpacked_fwd(q, kv, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
-                                  out=None, lse=None, stream=None):
+                                  out=None, lse=None, stream=None, layout="contiguous"):
     """q: (total, h, d), kv: (total, 2, h, d).  Returns (out (total, h, d), lse (h, total))."""
     if kv.dim() != 4 or kv.shape[1] != 2:
         raise ValueError("kv must be (total, 2, h, d)")
     return ring_attn_varlen_fwd(q, kv[:, 0], kv[:, 1], cu_seqlens, max_seqlen, n_shards, causal, softmax_scale,
-                                out=out, lse=lse, stream=stream)
+                                out=out, lse=lse, stream=stream, layout=layout)
 
 
 def ring_attn_varlen_kvpacked_bwd(dout, q, kv, out, lse, cu_seqlens, max_seqlen=None, n_shards=1, causal=True,
-                                  softmax_scale=None, dq=None, dkv=None, workspace=None, stream=None):
+                                  softmax_scale=None, dq=None, dkv=None, workspace=None, stream=None,
+                                  layout="contiguous"):
     """Gradient of ring_attn_varlen_kvpacked_fwd: (dq (total, h, d), dkv (total, 2, h, d))."""
     dq = torch.empty_like(q) if dq is None else dq
     dkv = torch.empty_like(kv) if dkv is None else dkv
     ring_attn_varlen_bwd(dout, q, kv[:, 0], kv[:, 1], out, lse, cu_seqlens, max_seqlen, n_shards, causal,
-                         softmax_scale, dq=dq, dk=dkv[:, 0], dv=dkv[:, 1], workspace=workspace, stream=stream)
+                         softmax_scale, dq=dq, dk=dkv[:, 0], dv=dkv[:, 1], workspace=workspace, stream=stream,
+                         layout=layout)
     return dq, dkv
+
+
+def ring_attn_varlen_permute(x, cu_seqlens, layout, n_shards, seq_dim=0, out=None, stream=None):
+    """Packed original order -> layout order along seq_dim for one cu_seqlens (bit copy)."""
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, x.device)
+    out = torch.empty_like(x) if out is None else out
+    a, b_ = _t(x), _t(out)
+    _check(lib.ring_attn_varlen_permute(ctypes.byref(a), ctypes.byref(b_), ctypes.c_void_p(dev.data_ptr()),
+                                        ctypes.c_void_p(host.data_ptr()), host.numel() - 1, _layout(layout),
+                                        int(n_shards), int(seq_dim), _stream(stream)), "ring_attn_varlen_permute")
+    return out
+
+
+def ring_attn_varlen_unpermute(y, cu_seqlens, layout, n_shards, seq_dim=0, out=None, stream=None):
+    """Layout order -> packed original order along seq_dim (bit copy)."""
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, y.device)
+    out = torch.empty_like(y) if out is None else out
+    a, b_ = _t(y), _t(out)
+    _check(lib.ring_attn_varlen_unpermute(ctypes.byref(a), ctypes.byref(b_), ctypes.c_void_p(dev.data_ptr()),
+                                          ctypes.c_void_p(host.data_ptr()), host.numel() - 1, _layout(layout),
+                                          int(n_shards), int(seq_dim), _stream(stream)), "ring_attn_varlen_unpermute")
+    return out
 
 
 def ring_attn_permute(x, layout, n_shards, seq_dim=2, out=None, stream=None):

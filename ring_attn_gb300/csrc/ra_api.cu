@@ -327,6 +327,17 @@ void* g_scratch_ptr[64] = {nullptr};
 
 ra_status static_scratch(void** out);
 
+// Varlen layouts: contiguous slices of the packed buffer, or the zigzag split
+// of every sequence (each length a multiple of 2 * n_shards).
+ra_status check_varlen_layout(int32_t layout, int32_t n_shards, const int32_t* cu_host, int32_t n_seqs) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG) return RA_ERR_UNSUPPORTED;
+  if (n_shards < 1) return RA_ERR_INVALID_ARG;
+  if (layout == RA_LAYOUT_ZIGZAG)
+    for (int32_t i = 0; i < n_seqs; ++i)
+      if ((cu_host[i + 1] - cu_host[i]) % (2 * n_shards) != 0) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
 ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs, int32_t max_seqlen,
                    long long* total) {
   if (!cu_dev || !cu_host || n_seqs < 1) return RA_ERR_INVALID_ARG;
@@ -542,13 +553,14 @@ ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q
 
 ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                                const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
-                               int32_t max_seqlen, int32_t n_shards, int32_t causal, float softmax_scale,
-                               ra_tensor* out, ra_tensor* lse, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+                               int32_t max_seqlen, int32_t layout, int32_t n_shards, int32_t causal,
+                               float softmax_scale, ra_tensor* out, ra_tensor* lse, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   (void)workspace;
   (void)workspace_bytes;
   long long total = 0;
   RA_TRY(check_cu(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, &total));
+  RA_TRY(check_varlen_layout(layout, n_shards, cu_seqlens_host, n_seqs));
   Bhsd vq, vk, vv, vo;
   RA_TRY(check_thd(q, total, &vq));
   RA_TRY(check_thd(k, total, &vk));
@@ -556,17 +568,18 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
   RA_TRY(check_thd(out, total, &vo));
   long long lsb, lsh, lss;
   RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
-  return fwd_common(vq, vk, vv, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, vo, 0,
+  return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, -1, vo, 0,
                     static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream);
 }
 
 ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                                const ra_tensor* out, const ra_tensor* lse, const int32_t* cu_seqlens_dev,
                                const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen,
-                               int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk,
-                               ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream) {
+                               int32_t layout, int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq,
+                               ra_tensor* dk, ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream) {
   long long total = 0;
   RA_TRY(check_cu(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, &total));
+  RA_TRY(check_varlen_layout(layout, n_shards, cu_seqlens_host, n_seqs));
   Bhsd vdo, vq, vk, vv, vo, vdq, vdk, vdv;
   RA_TRY(check_thd(dout, total, &vdo));
   RA_TRY(check_thd(q, total, &vq));
@@ -578,13 +591,13 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
   RA_TRY(check_thd(dv, total, &vdv));
   long long lsb, lsh, lss;
   RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
-  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss,
-                    RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, vdq, vdk, vdv, workspace,
-                    workspace_bytes, cu_seqlens_dev, n_seqs, stream);
+  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
+                    causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,
+                    stream);
 }
 
 static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t layout, int32_t n_shards,
-                                int32_t seq_dim, int inverse, void* stream) {
+                                int32_t seq_dim, int inverse, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
   if (!src || !dst || !src->data || !dst->data) return RA_ERR_INVALID_ARG;
   const int nd = src->ndim;
   if (nd < 1 || nd > 4 || dst->ndim != nd || src->dtype != dst->dtype) return RA_ERR_INVALID_ARG;
@@ -627,18 +640,42 @@ static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t la
   a.layout = layout;
   a.N = n_shards;
   a.inverse = inverse;
+  a.cu = cu_dev;
+  a.n_seqs = n_seqs;
   TimedLaunch tl(RA_KERNEL_PERMUTE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 
 ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, int32_t n_shards, int32_t seq_dim,
                             void* stream) {
-  return permute_common(x, y, layout, n_shards, seq_dim, 0, stream);
+  return permute_common(x, y, layout, n_shards, seq_dim, 0, nullptr, 0, stream);
 }
 
 ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,
                               void* stream) {
-  return permute_common(y, x, layout, n_shards, seq_dim, 1, stream);
+  return permute_common(y, x, layout, n_shards, seq_dim, 1, nullptr, 0, stream);
+}
+
+static ra_status varlen_permute_common(const ra_tensor* src, ra_tensor* dst, const int32_t* cu_dev,
+                                       const int32_t* cu_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
+                                       int32_t seq_dim, int inverse, void* stream) {
+  long long total = 0;
+  RA_TRY(check_cu(cu_dev, cu_host, n_seqs, INT32_MAX, &total));
+  RA_TRY(check_varlen_layout(layout, n_shards, cu_host, n_seqs));
+  if (!src || seq_dim < 0 || seq_dim >= src->ndim || src->shape[seq_dim] != total) return RA_ERR_INVALID_ARG;
+  return permute_common(src, dst, layout, n_shards, seq_dim, inverse, cu_dev, n_seqs, stream);
+}
+
+ra_status ring_attn_varlen_permute(const ra_tensor* x, ra_tensor* y, const int32_t* cu_seqlens_dev,
+                                   const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
+                                   int32_t seq_dim, void* stream) {
+  return varlen_permute_common(x, y, cu_seqlens_dev, cu_seqlens_host, n_seqs, layout, n_shards, seq_dim, 0, stream);
+}
+
+ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int32_t* cu_seqlens_dev,
+                                     const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
+                                     int32_t seq_dim, void* stream) {
+  return varlen_permute_common(y, x, cu_seqlens_dev, cu_seqlens_host, n_seqs, layout, n_shards, seq_dim, 1, stream);
 }
 
 size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards) {

@@ -304,13 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int j = k.j0 + jr;
     const bool valid_k = j < p.L;
-    const int gk = token_of(p.layout, p.N, p.L, k.s, valid_k ? j : k.j_last);
-    int rq_lo = 0, rq_hi = 0;  // varlen: queries [rq_lo, rq_hi) this key serves
-    if (p.cu) {
-      const int sg = segment_of(p.cu, p.n_seqs, gk);
-      rq_lo = p.causal ? gk : __ldg(p.cu + sg);
-      rq_hi = __ldg(p.cu + sg + 1);
-    }
+    const int gk = tok(p, k.s, valid_k ? j : k.j_last);
+    int rq_lo = 0, rq_hi = 0;  // varlen: the queries this key serves (see key_query_bounds)
+    if (p.cu) key_query_bounds(p, gk, rq_lo, rq_hi);
     bool ok = true;
     int i = 0;
     walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
@@ -639,13 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int i = i0 + row;
     const bool valid = i < p.L;
-    const int gq = token_of(p.layout, p.N, p.L, r, valid ? i : max(qr.i_last, 0));
-    int rk_lo = 0, rk_hi = 0;  // varlen: this row's allowed keys [rk_lo, rk_hi)
-    if (p.cu) {
-      const int sg = segment_of(p.cu, p.n_seqs, gq);
-      rk_lo = __ldg(p.cu + sg);
-      rk_hi = p.causal ? gq + 1 : __ldg(p.cu + sg + 1);
-    }
+    const int gq = tok(p, r, valid ? i : max(qr.i_last, 0));
+    int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
+    if (p.cu) row_key_bounds(p, gq, rk_lo, rk_hi);
     // this row's statistics, negated (padding rows: -lse2 = -inf, -D = 0, so P = dS = 0)
     const long long srow = (((long long)b * p.H + h) * p.N + r) * p.stat_L + i;
     const uint64_t nl2 = f32x2(__ldg(p.nlse2 + srow), __ldg(p.nlse2 + srow));

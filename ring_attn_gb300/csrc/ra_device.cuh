@@ -379,6 +379,34 @@ __device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs
   return lo;
 }
 
+// Zigzag varlen: sequence k (tokens [cu_k, cu_k1), a multiple of 2N) is cut
+// into 2N chunks of c = (cu_k1 - cu_k) / 2N tokens; every shard holds chunk r
+// then chunk 2N-1-r of each sequence in turn, so sequence k occupies local
+// positions [cu_k / N, cu_k1 / N) of every shard, in increasing token order.
+__device__ __forceinline__ int vz_token_in(int cu_k, int cu_k1, int N, int r, int i) {
+  const int c = (cu_k1 - cu_k) / (2 * N);
+  const int o = i - cu_k / N;
+  return cu_k + (o < c ? r * c + o : (2 * N - 1 - r) * c + (o - c));
+}
+
+__device__ __forceinline__ int vz_token(const int* __restrict__ cu, int n_seqs, int N, int r, int i) {
+  const int k = segment_of(cu, n_seqs, i * N);  // cu[k] / N <= i < cu[k+1] / N
+  return vz_token_in(__ldg(cu + k), __ldg(cu + k + 1), N, r, i);
+}
+
+// Largest local index of shard s holding a token of sequence k (tokens
+// [cu_k, cu_k1)) that is <= g, or cu_k / N - 1 when there is none.
+__device__ __forceinline__ int vz_last_le(int cu_k, int cu_k1, int N, int s, int g) {
+  const int c = (cu_k1 - cu_k) / (2 * N);
+  const int base = cu_k / N;
+  const int o = g - cu_k;
+  if (o < s * c) return base - 1;
+  if (o < (s + 1) * c) return base + (o - s * c);
+  if (o < (2 * N - 1 - s) * c) return base + c - 1;
+  if (o < (2 * N - s) * c) return base + c + (o - (2 * N - 1 - s) * c);
+  return base + 2 * c - 1;
+}
+
 }  // namespace ra
 
 namespace ra {

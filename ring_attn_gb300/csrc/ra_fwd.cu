@@ -274,13 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     make_qrange(p, r, i0 + t * kTileM, kTileM, qt);
     const int i = i0 + t * kTileM + row;
     const bool valid = i < p.L;
-    const int gq = token_of(p.layout, p.N, p.L, r, valid ? i : max(qt.i_last, 0));
-    int rk_lo = 0, rk_hi = 0;  // varlen: this row's allowed keys [rk_lo, rk_hi)
-    if (p.cu) {
-      const int sg = segment_of(p.cu, p.n_seqs, gq);
-      rk_lo = __ldg(p.cu + sg);
-      rk_hi = p.causal ? gq + 1 : __ldg(p.cu + sg + 1);
-    }
+    const int gq = tok(p, r, valid ? i : max(qt.i_last, 0));
+    int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
+    if (p.cu) row_key_bounds(p, gq, rk_lo, rk_hi);
     float m_run = -INFINITY;  // running max, in log2 units (scores * scale * log2 e)
     float l_run = 0.f;        // running sum of exp2(x - m_run)
     bool ok = true;

@@ -104,6 +104,8 @@ struct PermuteArgs {
   int s, layout, N;
   int inverse;              // 0: dst[p] = src[g(p)]; 1: dst[g(p)] = src[p]
   int vpr_total;            // vectors per row (set by the launcher)
+  const int* cu;            // varlen cu_seqlens (device) or nullptr
+  int n_seqs;
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 

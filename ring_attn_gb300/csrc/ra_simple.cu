@@ -35,7 +35,10 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vp
     o /= a.outer_shape[2];
     const long long o1 = o % a.outer_shape[1];
     const long long o0 = o / a.outer_shape[1];
-    const long long g = token_of(a.layout, a.N, L, p / L, p % L);  // original token at position p
+    // original token at layout position p
+    const long long g = a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
+                        : a.layout == LAYOUT_ZIGZAG ? vz_token(a.cu, a.n_seqs, a.N, p / L, p % L)
+                                                    : p;
     const long long src_pos = a.inverse ? p : g;
     const long long dst_pos = a.inverse ? g : p;
     const long long so = o0 * a.src_outer_stride[0] + o1 * a.src_outer_stride[1] + o2 * a.src_outer_stride[2] +

@@ -3,23 +3,39 @@
 //
 // The ring order is the pages' (guijiagi.com "Ring Attention：突破百万 Token
 // 上下文的分布式注意力", "详细流程"): at step t, Q shard r meets KV shard
-// (r - t) mod N, and KV shard s meets Q shard (s + t) mod N.  token_of is
-// increasing inside every shard for all three layouts, so for causal masking
-// the allowed keys of a row are a prefix of each KV shard, the allowed queries
-// of a key a suffix of each Q shard, and a tile is empty, full or partial by
-// its corners.  Varlen (contiguous layout, one cu_seqlens) adds the segment
-// bounds.  P is any parameter struct with N, L, layout, causal, cu and n_seqs.
+// (r - t) mod N, and KV shard s meets Q shard (s + t) mod N.  The original
+// token of a local position is increasing inside every shard for all layouts,
+// so for causal masking the allowed keys of a row are a prefix of each KV
+// shard (within its sequence, for varlen), the allowed queries of a key a
+// suffix of each Q shard, and a tile is empty, full or partial by its corners.
+// Varlen takes one cu_seqlens over the packed buffer with the contiguous
+// layout (shards are slices of the packed buffer) or the zigzag layout applied
+// to every sequence (sequence k at local [cu[k]/N, cu[k+1]/N) of every shard).
+// P is any parameter struct with N, L, layout, causal, cu and n_seqs.
 #pragma once
 
 #include "ra_internal.h"
 
 namespace ra {
 
+template <class P>
+__device__ __forceinline__ bool vz(const P& p) {
+  return p.cu != nullptr && p.layout == LAYOUT_ZIGZAG;
+}
+
+// Original token of local position i of shard r.
+template <class P>
+__device__ __forceinline__ int tok(const P& p, int r, int i) {
+  if (vz(p)) return vz_token(p.cu, p.n_seqs, p.N, r, i);
+  return token_of(p.layout, p.N, p.L, r, i);
+}
+
 // Query rows [i0, i0 + rows) of Q shard r; the valid ones end at i_last.
 struct QRange {
   int r, i0, i_last;
   int gq_lo, gq_hi;    // original token indices of the first / last valid row
-  int key_lo, key_hi;  // varlen: keys any row may see (inclusive)
+  int key_lo, key_hi;  // contiguous varlen: keys any row may see (inclusive)
+  int seg_lo, seg_hi;  // varlen: segments of the first / last valid row
   int seg_single;      // varlen: the segment of every valid row, or -1
 };
 
@@ -29,15 +45,18 @@ __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows,
   q.i0 = i0;
   q.i_last = min(i0 + rows, p.L) - 1;
   const int ilo = min(i0, p.L - 1);
-  q.gq_lo = token_of(p.layout, p.N, p.L, r, ilo);
-  q.gq_hi = token_of(p.layout, p.N, p.L, r, max(q.i_last, ilo));
+  q.gq_lo = tok(p, r, ilo);
+  q.gq_hi = tok(p, r, max(q.i_last, ilo));
   q.key_lo = q.key_hi = 0;
+  q.seg_lo = q.seg_hi = 0;
   q.seg_single = -1;
   if (p.cu) {
     const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
     const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
     q.key_lo = __ldg(p.cu + sa);
     q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
+    q.seg_lo = sa;
+    q.seg_hi = sz;
     q.seg_single = sa == sz ? sa : -1;
   }
 }
@@ -46,8 +65,17 @@ __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows,
 template <class P>
 __device__ __forceinline__ void kv_range(const P& p, const QRange& q, int s, int nkt, int& lo, int& hi) {
   if (p.cu) {
-    const int base = s * p.L;
-    int jlo = q.key_lo - base, jhi = q.key_hi - base;
+    int jlo, jhi;  // local key positions of shard s, inclusive
+    if (vz(p)) {
+      // keys of the rows' sequences up to the last row's token (local order is token order)
+      const int ca = __ldg(p.cu + q.seg_lo), cz = __ldg(p.cu + q.seg_hi), cz1 = __ldg(p.cu + q.seg_hi + 1);
+      jlo = ca / p.N;
+      jhi = p.causal ? vz_last_le(cz, cz1, p.N, s, q.gq_hi) : cz1 / p.N - 1;
+    } else {
+      const int base = s * p.L;
+      jlo = q.key_lo - base;
+      jhi = q.key_hi - base;
+    }
     if (jlo < 0) jlo = 0;
     if (jhi > p.L - 1) jhi = p.L - 1;
     if (jlo > jhi) {
@@ -76,8 +104,12 @@ __device__ __forceinline__ bool kv_tile_full(const P& p, const QRange& q, int s,
   if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
   if (p.cu) {
     if (q.seg_single < 0) return false;
-    const int base = s * p.L + j0;
     const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
+    if (vz(p)) {
+      if (j0 < slo / p.N || j0 + kTileN > shi / p.N) return false;
+      return !p.causal || q.gq_lo >= vz_token_in(slo, shi, p.N, s, j0 + kTileN - 1);
+    }
+    const int base = s * p.L + j0;
     if (base < slo || base + kTileN > shi) return false;
     return !p.causal || q.gq_lo >= base + kTileN - 1;
   }
@@ -97,8 +129,18 @@ __device__ __forceinline__ void walk_kv_tiles(const P& p, const QRange& q, int n
   }
 }
 
-// Allowed key columns [c_lo, c_hi) of a query row (token gq, varlen key bounds
-// [rk_lo, rk_hi)) in key tile kt of shard s.
+// Per-row bounds for the varlen windows below: the row's key bounds in
+// tokens [rk_lo, rk_hi) for the contiguous layout (the causal bound folded
+// in), or its sequence [cu[k], cu[k+1]) for the zigzag layout.
+template <class P>
+__device__ __forceinline__ void row_key_bounds(const P& p, int gq, int& rk_lo, int& rk_hi) {
+  const int sg = segment_of(p.cu, p.n_seqs, gq);
+  rk_lo = __ldg(p.cu + sg);
+  rk_hi = (p.causal && !vz(p)) ? gq + 1 : __ldg(p.cu + sg + 1);
+}
+
+// Allowed key columns [c_lo, c_hi) of a query row (token gq, varlen bounds
+// [rk_lo, rk_hi) from row_key_bounds) in key tile kt of shard s.
 template <class P>
 __device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, int rk_hi, int s, int kt, int& c_lo,
                                                int& c_hi) {
@@ -107,8 +149,15 @@ __device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, in
   c_lo = 0;
   c_hi = jlim;
   if (p.cu) {
-    const int base = s * p.L + j0;
-    const int lo = rk_lo - base, hi = rk_hi - base;
+    int lo, hi;  // allowed local keys [lo, hi) of shard s, relative to the tile
+    if (vz(p)) {
+      lo = rk_lo / p.N - j0;
+      hi = (p.causal ? vz_last_le(rk_lo, rk_hi, p.N, s, gq) + 1 : rk_hi / p.N) - j0;
+    } else {
+      const int base = s * p.L + j0;
+      lo = rk_lo - base;
+      hi = rk_hi - base;
+    }
     c_lo = lo < 0 ? 0 : (lo > kTileN ? kTileN : lo);
     c_hi = hi < 0 ? 0 : (hi > jlim ? jlim : hi);
   } else if (p.causal) {
@@ -121,7 +170,8 @@ __device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, in
 struct KRange {
   int s, j0, j_last;
   int gk_lo, gk_hi;
-  int qry_lo, qry_hi;  // varlen: queries any key of the tile may serve (inclusive)
+  int qry_lo, qry_hi;  // contiguous varlen: queries any key of the tile may serve (inclusive)
+  int seg_lo, seg_hi;  // varlen: segments of the first / last valid key
   int seg_single;
 };
 
@@ -130,15 +180,18 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
   k.s = s;
   k.j0 = j0;
   k.j_last = min(j0 + kTileN, p.L) - 1;
-  k.gk_lo = token_of(p.layout, p.N, p.L, s, j0);
-  k.gk_hi = token_of(p.layout, p.N, p.L, s, k.j_last);
+  k.gk_lo = tok(p, s, j0);
+  k.gk_hi = tok(p, s, k.j_last);
   k.qry_lo = k.qry_hi = 0;
+  k.seg_lo = k.seg_hi = 0;
   k.seg_single = -1;
   if (p.cu) {
     const int sa = segment_of(p.cu, p.n_seqs, k.gk_lo);
     const int sz = segment_of(p.cu, p.n_seqs, k.gk_hi);
     k.qry_lo = p.causal ? k.gk_lo : __ldg(p.cu + sa);
     k.qry_hi = __ldg(p.cu + sz + 1) - 1;
+    k.seg_lo = sa;
+    k.seg_hi = sz;
     k.seg_single = sa == sz ? sa : -1;
   }
 }
@@ -147,8 +200,17 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
 template <int QT, class P>
 __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int nqt, int& lo, int& hi) {
   if (p.cu) {
-    const int base = r * p.L;
-    int ilo = k.qry_lo - base, ihi = k.qry_hi - base;
+    int ilo, ihi;  // local query positions of shard r, inclusive
+    if (vz(p)) {
+      // queries of the keys' sequences from the first key's token on
+      const int ca = __ldg(p.cu + k.seg_lo), ca1 = __ldg(p.cu + k.seg_lo + 1);
+      ilo = p.causal ? vz_last_le(ca, ca1, p.N, r, k.gk_lo - 1) + 1 : ca / p.N;
+      ihi = __ldg(p.cu + k.seg_hi + 1) / p.N - 1;
+    } else {
+      const int base = r * p.L;
+      ilo = k.qry_lo - base;
+      ihi = k.qry_hi - base;
+    }
     if (ilo < 0) ilo = 0;
     if (ihi > p.L - 1) ihi = p.L - 1;
     if (ilo > ihi) {
@@ -176,8 +238,12 @@ __device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, 
   if (i0 + QT > p.L || k.j0 + kTileN > p.L) return false;
   if (p.cu) {
     if (k.seg_single < 0) return false;
-    const int base = r * p.L + i0;
     const int slo = __ldg(p.cu + k.seg_single), shi = __ldg(p.cu + k.seg_single + 1);
+    if (vz(p)) {
+      if (i0 < slo / p.N || i0 + QT > shi / p.N) return false;
+      return !p.causal || vz_token_in(slo, shi, p.N, r, i0) >= k.gk_hi;
+    }
+    const int base = r * p.L + i0;
     if (base < slo || base + QT > shi) return false;
     return !p.causal || base >= k.gk_hi;
   }
@@ -197,8 +263,18 @@ __device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nq
   }
 }
 
-// Allowed query columns [c_lo, c_hi) of a key row (token gk, varlen query bounds
-// [rq_lo, rq_hi)) in query tile qt (QT rows) of shard r.
+// Per-key bounds for key_query_window: the queries a key serves in tokens
+// [rq_lo, rq_hi) for the contiguous layout (the causal bound folded in), or
+// its sequence [cu[k], cu[k+1]) for the zigzag layout.
+template <class P>
+__device__ __forceinline__ void key_query_bounds(const P& p, int gk, int& rq_lo, int& rq_hi) {
+  const int sg = segment_of(p.cu, p.n_seqs, gk);
+  rq_lo = (p.causal && !vz(p)) ? gk : __ldg(p.cu + sg);
+  rq_hi = __ldg(p.cu + sg + 1);
+}
+
+// Allowed query columns [c_lo, c_hi) of a key row (token gk, varlen bounds
+// [rq_lo, rq_hi) from key_query_bounds) in query tile qt (QT rows) of shard r.
 template <int QT, class P>
 __device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int gk, int rq_lo, int rq_hi, int r, int qt,
                                                  int& c_lo, int& c_hi) {
@@ -208,8 +284,15 @@ __device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int g
   const int ilim = min(QT, p.L - i0);
   c_hi = ilim;
   if (p.cu) {
-    const int base = r * p.L + i0;
-    const int lo = rq_lo - base, hi = rq_hi - base;
+    int lo, hi;  // allowed local queries [lo, hi) of shard r, relative to the tile
+    if (vz(p)) {
+      lo = (p.causal ? vz_last_le(rq_lo, rq_hi, p.N, r, gk - 1) + 1 : rq_lo / p.N) - i0;
+      hi = rq_hi / p.N - i0;
+    } else {
+      const int base = r * p.L + i0;
+      lo = rq_lo - base;
+      hi = rq_hi - base;
+    }
     c_lo = lo < 0 ? 0 : (lo > QT ? QT : lo);
     c_hi = hi < 0 ? 0 : (hi > ilim ? ilim : hi);
   } else if (p.causal) {

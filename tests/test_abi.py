@@ -124,17 +124,33 @@ def test_varlen_rejects_bad_cu_seqlens(lib):
     q = _fake((64, 2, 64))
     lse = _fake((2, 64), ra.RA_FP32)
 
-    def call(cu, n, maxlen=64):
+    def call(cu, n, maxlen=64, layout=0):
         arr = (ctypes.c_int32 * len(cu))(*cu)
         return lib.ring_attn_varlen_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), ctypes.c_void_p(0x1000),
-                                        ctypes.cast(arr, ctypes.c_void_p), n, maxlen, 2, 1, 0.125, ctypes.byref(q),
-                                        ctypes.byref(lse), None, 0, None)
+                                        ctypes.cast(arr, ctypes.c_void_p), n, maxlen, layout, 2, 1, 0.125,
+                                        ctypes.byref(q), ctypes.byref(lse), None, 0, None)
 
     assert call([1, 64], 1) == 1           # cu[0] != 0
     assert call([0, 40, 30, 64], 3) == 1   # decreasing
     assert call([0, 40, 64], 2, maxlen=10) == 1  # max_seqlen too small
     assert call([0, 40, 60], 2) == 1       # total does not match the tensors
     assert call([0, 64], 0) == 1           # no sequence
+    assert call([0, 42, 64], 2, layout=1) == 1   # zigzag: 42 is not a multiple of 2 * n_shards
+    assert call([0, 40, 64], 2, layout=2) == 2   # stripe varlen: not supported
+
+
+def test_varlen_permute_rejects_bad_arguments(lib):
+    x = _fake((64, 2, 64))
+
+    def call(cu, n, layout, n_shards=2, seq_dim=0):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        return lib.ring_attn_varlen_permute(ctypes.byref(x), ctypes.byref(x), ctypes.c_void_p(0x1000),
+                                            ctypes.cast(arr, ctypes.c_void_p), n, layout, n_shards, seq_dim, None)
+
+    assert call([0, 40, 60], 2, 1) == 1    # total does not match the sequence axis
+    assert call([0, 42, 64], 2, 1) == 1    # zigzag length not a multiple of 2 * n_shards
+    assert call([0, 40, 64], 2, 2) == 2    # stripe varlen: not supported
+    assert call([0, 40, 64], 2, 1, seq_dim=3) == 1
 
 
 def test_lse_merge_rejects_bad_shapes(lib):

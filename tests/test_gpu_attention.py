@@ -184,6 +184,60 @@ def test_varlen_fwd_bwd(ra, lens, n, causal, packed):
         assert_close(name, back(got), r)
 
 
+# ----------------------------------------------------------------------------- zigzag varlen
+@pytest.mark.parametrize("lens,n", [
+    ([4, 132, 260, 0, 508], 2),
+    ([128, 24, 320, 8], 4),
+    ([6 * 20, 6 * 7, 6 * 50], 3),
+])
+def test_varlen_zigzag_permute_bit_exact(ra, lens, n):
+    cu = cu_seqlens(lens)
+    total = cu[-1]
+    g = oracle.varlen_token_of_position("zigzag", n, cu)
+    x16 = make_qkv(1, 3, total, 64, 11, with_do=False)["q"][0].transpose(0, 1).contiguous()  # (total, h, d)
+    y = ra.ring_attn_varlen_permute(x16.cuda(), cu, "zigzag", n, seq_dim=0).cpu()
+    assert torch.equal(y.view(torch.int16), x16[torch.from_numpy(g)].view(torch.int16))
+    back = ra.ring_attn_varlen_unpermute(y.cuda(), cu, "zigzag", n, seq_dim=0).cpu()
+    assert torch.equal(back.view(torch.int16), x16.view(torch.int16))
+    x32 = torch.randn(2, total, generator=torch.Generator().manual_seed(5))  # (h, total) fp32, seq_dim 1
+    y32 = ra.ring_attn_varlen_permute(x32.cuda(), cu, "zigzag", n, seq_dim=1).cpu()
+    assert torch.equal(y32, x32[:, torch.from_numpy(g)])
+    ident = ra.ring_attn_varlen_permute(x16.cuda(), cu, "contiguous", n, seq_dim=0).cpu()
+    assert torch.equal(ident.view(torch.int16), x16.view(torch.int16))
+
+
+@pytest.mark.parametrize("lens,n", [
+    ([4, 132, 260, 0, 508], 2),            # a 4-token sequence, tile-crossing ones, an empty one
+    ([128, 24, 320, 8], 4),
+    ([16 * 70], 8),                        # one sequence: the batched zigzag split
+    ([6 * 20, 6 * 7, 6 * 50, 6 * 1], 3),
+    ([8] * 30 + [8 * 64], 4),              # many tiny sequences inside one tile
+])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d):
+    h = 2
+    cu = cu_seqlens(lens)
+    x = make_qkv(1, h, cu[-1], d, 300 + len(lens) + n, with_do=True)
+    scale = d ** -0.5
+    g = {k: ra.ring_attn_varlen_permute(v[0].transpose(0, 1).contiguous().cuda(), cu, "zigzag", n, seq_dim=0)
+         for k, v in x.items()}
+    out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, causal, scale, layout="zigzag")
+    dq, dk, dv = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu, None, n, causal, scale,
+                                         layout="zigzag")
+    check_no_device_error(ra)
+    ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, causal, cu_seqlens=cu)
+    ref_g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, cu_seqlens=cu)
+
+    def back(t, seq_dim=0):
+        return ra.ring_attn_varlen_unpermute(t.contiguous(), cu, "zigzag", n, seq_dim=seq_dim).cpu()
+
+    assert_close("out", back(out).transpose(0, 1).unsqueeze(0), ref_o)
+    assert_lse_close("lse", back(lse, 1).unsqueeze(0), ref_l)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref_g):
+        assert_close(name, back(got).transpose(0, 1).unsqueeze(0), r)
+
+
 # ----------------------------------------------------------------------------- bounded waits
 def test_bounded_wait_reports_timeout_and_context_survives(ra):
     """The producer is told to skip the Q load, so the MMA and softmax warps'
