@@ -117,11 +117,12 @@ enum DkdvBar {
   E_TEARDOWN = 14
 };
 
-template <int D>
+// VL: varlen instantiation (FwdParamsT / BwdParamsT carry it as kVarlen).
+template <int D, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                     const BwdParams p) {
+                     const BwdParamsT<VL> p) {
   using LY = DkdvLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid_k = j < p.L;
     const int gk = tok(p, k.s, valid_k ? j : k.j_last);
     int rq_lo = 0, rq_hi = 0;  // varlen: the queries this key serves (see key_query_bounds)
-    if (p.cu) key_query_bounds(p, gk, rq_lo, rq_hi);
+    if (cu_of(p)) key_query_bounds(p, gk, rq_lo, rq_hi);
     bool ok = true;
     int i = 0;
     walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
@@ -466,11 +467,11 @@ enum DqBar {
   F_TEARDOWN = 17
 };
 
-template <int D>
+template <int D, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                   const BwdParams p) {
+                   const BwdParamsT<VL> p) {
   using LY = DqLayout<D>;
   constexpr int KS = LY::kKStages, VS = LY::kVStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -637,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = i < p.L;
     const int gq = tok(p, r, valid ? i : max(qr.i_last, 0));
     int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
-    if (p.cu) row_key_bounds(p, gq, rk_lo, rk_hi);
+    if (cu_of(p)) row_key_bounds(p, gq, rk_lo, rk_hi);
     // this row's statistics, negated (padding rows: -lse2 = -inf, -D = 0, so P = dS = 0)
     const long long srow = (((long long)b * p.H + h) * p.N + r) * p.stat_L + i;
     const uint64_t nl2 = f32x2(__ldg(p.nlse2 + srow), __ldg(p.nlse2 + srow));
@@ -751,27 +752,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, bool VL>
+cudaError_t launch_bwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st) {
+  BwdParamsT<VL> pv;
+  static_cast<BwdParams&>(pv) = p;
   if (which == 0) {
     // the register split inside the kernel is only safe with the launch allocation it was sized for
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, ring_dkdv_kernel<D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, ring_dkdv_kernel<D, VL>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kDkdvLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(ring_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::kAlloc);
+    e = cudaFuncSetAttribute(ring_dkdv_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.N * p.n_ktiles), (unsigned)(p.B * p.H));
-    ring_dkdv_kernel<D><<<grid, kThreads, DkdvLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    ring_dkdv_kernel<D, VL><<<grid, kThreads, DkdvLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);
   } else {
-    cudaError_t e =
-        cudaFuncSetAttribute(ring_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(ring_dq_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.N * p.n_qtiles), (unsigned)(p.B * p.H));
-    ring_dq_kernel<D><<<grid, kThreads, DqLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    ring_dq_kernel<D, VL><<<grid, kThreads, DqLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);
   }
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st) {
+  return p.cu ? launch_bwd_v<D, true>(tq, tk, tv, tdo, p, which, st)
+              : launch_bwd_v<D, false>(tq, tk, tv, tdo, p, which, st);
 }
 
 }  // namespace

@@ -83,17 +83,18 @@ enum FwdBar {
 };
 
 // The CTA's key tiles, in ring order (all ring steps, or the one the step mode asks for).
-template <class F>
-__device__ __forceinline__ void walk_tiles(const FwdParams& p, const QRange& q, int nkt, F&& f) {
+template <class P, class F>
+__device__ __forceinline__ void walk_tiles(const P& p, const QRange& q, int nkt, F&& f) {
   const int t0 = p.step < 0 ? 0 : p.step;
   const int t1 = p.step < 0 ? p.N : p.step + 1;
   walk_kv_tiles(p, q, nkt, t0, t1, f);
 }
 
-template <int D>
+// VL: varlen instantiation (FwdParamsT / BwdParamsT carry it as kVarlen).
+template <int D, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const FwdParamsT<VL> p) {
   using LY = FwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = i < p.L;
     const int gq = tok(p, r, valid ? i : max(qt.i_last, 0));
     int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
-    if (p.cu) row_key_bounds(p, gq, rk_lo, rk_hi);
+    if (cu_of(p)) row_key_bounds(p, gq, rk_lo, rk_hi);
     float m_run = -INFINITY;  // running max, in log2 units (scores * scale * log2 e)
     float l_run = 0.f;        // running sum of exp2(x - m_run)
     bool ok = true;
@@ -434,22 +435,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+template <int D, bool VL>
+cudaError_t launch_fwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                          cudaStream_t st) {
   using LY = FwdLayout<D>;
   // the register split inside the kernel is only safe with the launch
   // allocation it was sized for
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, ring_fwd_kernel<D>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, ring_fwd_kernel<D, VL>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(ring_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
+  e = cudaFuncSetAttribute(ring_fwd_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid((unsigned)(p.N * n_pairs), (unsigned)(p.B * p.H));
-  ring_fwd_kernel<D><<<grid, kThreads, LY::kAlloc, st>>>(tq, tk, tv, p);
+  FwdParamsT<VL> pv;
+  static_cast<FwdParams&>(pv) = p;
+  ring_fwd_kernel<D, VL><<<grid, kThreads, LY::kAlloc, st>>>(tq, tk, tv, pv);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                         cudaStream_t st) {
+  return p.cu ? launch_fwd_v<D, true>(tq, tk, tv, p, st) : launch_fwd_v<D, false>(tq, tk, tv, p, st);
 }
 
 }  // namespace

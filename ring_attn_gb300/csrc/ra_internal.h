@@ -48,6 +48,17 @@ struct BwdParams {
   DevCtl ctl;
 };
 
+// The kernel parameters with a compile-time varlen flag: the batched kernels
+// are instantiated with kVarlen = false, so every varlen branch folds away.
+template <bool VL>
+struct FwdParamsT : FwdParams {
+  static constexpr bool kVarlen = VL;
+};
+template <bool VL>
+struct BwdParamsT : BwdParams {
+  static constexpr bool kVarlen = VL;
+};
+
 // Strided 4-D view of a tensor whose last dimension is contiguous.
 struct View4 {
   void* data;

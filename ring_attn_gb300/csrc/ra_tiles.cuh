@@ -11,16 +11,22 @@
 // Varlen takes one cu_seqlens over the packed buffer with the contiguous
 // layout (shards are slices of the packed buffer) or the zigzag layout applied
 // to every sequence (sequence k at local [cu[k]/N, cu[k+1]/N) of every shard).
-// P is any parameter struct with N, L, layout, causal, cu and n_seqs.
+// P is FwdParamsT or BwdParamsT (N, L, layout, causal, cu, n_seqs and kVarlen).
 #pragma once
 
 #include "ra_internal.h"
 
 namespace ra {
 
+// cu_seqlens of a varlen call; nullptr (known at compile time) in batched kernels.
+template <class P>
+__device__ __forceinline__ const int* cu_of(const P& p) {
+  return P::kVarlen ? p.cu : nullptr;
+}
+
 template <class P>
 __device__ __forceinline__ bool vz(const P& p) {
-  return p.cu != nullptr && p.layout == LAYOUT_ZIGZAG;
+  return cu_of(p) != nullptr && p.layout == LAYOUT_ZIGZAG;
 }
 
 // Original token of local position i of shard r.
@@ -50,7 +56,7 @@ __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows,
   q.key_lo = q.key_hi = 0;
   q.seg_lo = q.seg_hi = 0;
   q.seg_single = -1;
-  if (p.cu) {
+  if (cu_of(p)) {
     const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
     const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
     q.key_lo = __ldg(p.cu + sa);
@@ -64,7 +70,7 @@ __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows,
 // Key-tile range [lo, hi) of KV shard s that can hold a key allowed for some row of q.
 template <class P>
 __device__ __forceinline__ void kv_range(const P& p, const QRange& q, int s, int nkt, int& lo, int& hi) {
-  if (p.cu) {
+  if (cu_of(p)) {
     int jlo, jhi;  // local key positions of shard s, inclusive
     if (vz(p)) {
       // keys of the rows' sequences up to the last row's token (local order is token order)
@@ -102,7 +108,7 @@ template <class P>
 __device__ __forceinline__ bool kv_tile_full(const P& p, const QRange& q, int s, int kt) {
   const int j0 = kt * kTileN;
   if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
-  if (p.cu) {
+  if (cu_of(p)) {
     if (q.seg_single < 0) return false;
     const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
     if (vz(p)) {
@@ -148,7 +154,7 @@ __device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, in
   const int jlim = min(kTileN, p.L - j0);
   c_lo = 0;
   c_hi = jlim;
-  if (p.cu) {
+  if (cu_of(p)) {
     int lo, hi;  // allowed local keys [lo, hi) of shard s, relative to the tile
     if (vz(p)) {
       lo = rk_lo / p.N - j0;
@@ -185,7 +191,7 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
   k.qry_lo = k.qry_hi = 0;
   k.seg_lo = k.seg_hi = 0;
   k.seg_single = -1;
-  if (p.cu) {
+  if (cu_of(p)) {
     const int sa = segment_of(p.cu, p.n_seqs, k.gk_lo);
     const int sz = segment_of(p.cu, p.n_seqs, k.gk_hi);
     k.qry_lo = p.causal ? k.gk_lo : __ldg(p.cu + sa);
@@ -199,7 +205,7 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
 // Query-tile range [lo, hi) (tiles of QT rows) of Q shard r that holds a query some key of k serves.
 template <int QT, class P>
 __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int nqt, int& lo, int& hi) {
-  if (p.cu) {
+  if (cu_of(p)) {
     int ilo, ihi;  // local query positions of shard r, inclusive
     if (vz(p)) {
       // queries of the keys' sequences from the first key's token on
@@ -236,7 +242,7 @@ template <int QT, class P>
 __device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, int qt) {
   const int i0 = qt * QT;
   if (i0 + QT > p.L || k.j0 + kTileN > p.L) return false;
-  if (p.cu) {
+  if (cu_of(p)) {
     if (k.seg_single < 0) return false;
     const int slo = __ldg(p.cu + k.seg_single), shi = __ldg(p.cu + k.seg_single + 1);
     if (vz(p)) {
@@ -283,7 +289,7 @@ __device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int g
   const int i0 = qt * QT;
   const int ilim = min(QT, p.L - i0);
   c_hi = ilim;
-  if (p.cu) {
+  if (cu_of(p)) {
     int lo, hi;  // allowed local queries [lo, hi) of shard r, relative to the tile
     if (vz(p)) {
       lo = (p.causal ? vz_last_le(rq_lo, rq_hi, p.N, r, gk - 1) + 1 : rq_lo / p.N) - i0;
