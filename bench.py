@@ -215,6 +215,47 @@ def _shrink(s, h):
 
 
 # ----------------------------------------------------------------------------- our arm
+def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3):
+    """fwd + bwd of a packed varlen workload, inputs resident in layout order,
+    timed with CUDA events around `steps` steps on the current stream."""
+    from workload import WORKLOADS, cu_seqlens, make_workload_inputs
+
+    w = WORKLOADS[wid]
+    cu = torch.tensor(cu_seqlens(w.seq_lengths()), dtype=torch.int32)
+    x = make_workload_inputs(w, device=str(dev))
+    g = {n: ra.ring_attn_varlen_permute(t[0].contiguous(), cu, w.layout, w.n_shards, seq_dim=1) for n, t in x.items()}
+    del x
+    out = torch.empty_like(g["q"])
+    lse = torch.empty((w.h, w.s), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+    ws = torch.empty(ra.ring_attn_workspace_size(1, 1, w.h, w.s, w.d, w.n_shards), dtype=torch.uint8, device=dev)
+    cu_host = cu.contiguous()
+
+    def step():
+        ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu_host, None, w.n_shards, w.causal, w.scale, out=out, lse=lse,
+                                layout=w.layout)
+        ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu_host, None, w.n_shards, w.causal,
+                                w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, layout=w.layout)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    st, info = ra.ring_attn_check_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} info {info:#x} in the varlen leg")
+    tf = 2.5 * w.fwd_flops() / (ms * 1e-3) / 1e12
+    return {"workload": f"{w.name}: h{w.h} total {w.s} d{w.d}, {w.varlen_seqs} seqs, {w.n_shards} {w.layout} shards",
+            "ms_per_step": ms, "tflops": tf, "frac_of_peak": tf / peaks["bf16_sustained"],
+            "flop_convention": "fwd = sum_k 4*h*L_k^2*d/2; fwd+bwd = 2.5 x fwd"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -376,6 +417,10 @@ def main():
     result["permute"] = {"gbs": p_bytes / (p_ms / p_n * 1e-3) / 1e9, "ms": p_ms / p_n,
                          "frac_of_hbm": p_bytes / (p_ms / p_n * 1e-3) / 1e9 / peaks["hbm"]}
     ra.ring_attn_timing_enable(False)
+
+    # ---- varlen workloads (64 packed sequences, one cu_seqlens), contiguous and zigzag shards
+    if not (args.seq or args.heads):
+        result["varlen"] = {k: _varlen_leg(ra, torch, k, peaks, dev) for k in (5, 6)}
 
     # ---- e2e: host buffers in original order -> device -> permute -> fwd -> bwd -> unpermute -> host
     if not args.no_e2e:

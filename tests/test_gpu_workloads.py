@@ -1,4 +1,4 @@
-"""The five benchmark workloads at full size, in the launch configuration that
+"""The benchmark workloads at full size, in the launch configuration that
 bench.py times (fused ring forward, then the ring backward with a caller
 workspace), checked against the fp64 oracle on sampled outputs it can afford,
 plus properties that hold at any size:
@@ -42,14 +42,19 @@ def _run(ra, w):
         lens = w.seq_lengths()
         cu = cu_seqlens(lens)
         res["cu"] = cu
-        g = {k: v[0].contiguous() for k, v in x.items()}  # (h, total, d)
         cu_t = torch.tensor(cu, dtype=torch.int32)
-        out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu_t, None, w.n_shards, w.causal, scale)
-        res["out"], res["lse"] = out.unsqueeze(0), lse.unsqueeze(0)
+        # (h, total, d) in layout order (the identity for contiguous shards)
+        g = {k: ra.ring_attn_varlen_permute(v[0].contiguous(), cu_t, w.layout, w.n_shards, seq_dim=1)
+             for k, v in x.items()}
+        back = lambda t: ra.ring_attn_varlen_unpermute(t, cu_t, w.layout, w.n_shards, seq_dim=1)  # noqa: E731
+        out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu_t, None, w.n_shards, w.causal, scale,
+                                           layout=w.layout)
+        res["out"], res["lse"] = back(out).unsqueeze(0), back(lse).unsqueeze(0)
         if w.backward:
             dq, dk, dv = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu_t, None, w.n_shards,
-                                                 w.causal, scale)
-            res["dq"], res["dk"], res["dv"] = dq.unsqueeze(0), dk.unsqueeze(0), dv.unsqueeze(0)
+                                                 w.causal, scale, layout=w.layout)
+            res["dq"], res["dk"], res["dv"] = back(dq).unsqueeze(0), back(dk).unsqueeze(0), back(dv).unsqueeze(0)
+        del g
     else:
         g = {k: ra.ring_attn_permute(v, w.layout, w.n_shards) for k, v in x.items()}
         out = torch.empty_like(g["q"])
@@ -148,10 +153,11 @@ def test_causal_fwd_bwd_full_size(ra, wid):
         assert torch.isfinite(res[n].float()).all(), n
 
 
-def test_varlen_fwd_bwd_full_size(ra):
-    w = WORKLOADS[5]
+@pytest.mark.parametrize("wid", [5, 6])
+def test_varlen_fwd_bwd_full_size(ra, wid):
+    w = WORKLOADS[wid]
     res = _run(ra, w)
-    _check_rows(w, res, heads=[0, 31], n_rows=48, seed=5)
+    _check_rows(w, res, heads=[0, 31], n_rows=48, seed=wid)
     cu = res["cu"]
     rng = np.random.default_rng(55)
     segs = rng.choice(len(cu) - 1, size=3, replace=False)

@@ -37,6 +37,7 @@ class Workload:
     varlen_seqs: int = 0  # >0: packed sequences with one cu_seqlens (b must be 1)
     varlen_seed: int = 2000
     lengths: tuple = field(default=(), compare=False)
+    length_multiple: int = 1  # every packed length a multiple of this (zigzag varlen needs 2N)
 
     @property
     def scale(self) -> float:
@@ -47,9 +48,16 @@ class Workload:
         return self.s // self.n_shards
 
     def seq_lengths(self) -> list[int]:
+        """Packed lengths: the log-uniform recipe of varlen_lengths; with a length
+        multiple m, the same draw at a resolution of m tokens (lengths m * l_k
+        with l_k = varlen_lengths(n, s / m, seed, 512 / m, 16384 / m))."""
         if not self.varlen_seqs:
             return []
-        return varlen_lengths(self.varlen_seqs, self.s, self.varlen_seed)
+        m = self.length_multiple
+        if m == 1:
+            return varlen_lengths(self.varlen_seqs, self.s, self.varlen_seed)
+        units = varlen_lengths(self.varlen_seqs, self.s // m, self.varlen_seed, 512.0 / m, 16384.0 / m)
+        return [m * u for u in units]
 
     def fwd_flops(self) -> float:
         """Causal-adjusted forward FLOP: 4*b*h*s_q*s_k*d, halved when causal.
@@ -72,6 +80,10 @@ WORKLOADS = {
     4: Workload("causal_stripe_fwdbwd_h16_s128k", 1, 16, 131072, 128, "stripe", 8, True, True, 1004),
     5: Workload("varlen_causal_fwdbwd_64seq_128k", 1, 32, 131072, 128, "contiguous", 8, True, True, 1005,
                 varlen_seqs=64),
+    # zigzag varlen (the zigzag split of every packed sequence): workload 5's
+    # recipe with lengths in multiples of 2N = 16 tokens
+    6: Workload("varlen_zigzag_causal_fwdbwd_64seq_128k", 1, 32, 131072, 128, "zigzag", 8, True, True, 1006,
+                varlen_seqs=64, length_multiple=16),
 }
 
 
