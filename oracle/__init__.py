@@ -16,6 +16,7 @@ from .attention import (  # noqa: F401
     attention_rows,
     block_attention,
     key_grads,
+    llama3_rank_attention,
     lse_merge,
     online_softmax_attention,
     permute,

@@ -10,6 +10,8 @@ Pages cited (by title and section):
              "在线 Softmax：关键技巧" (the online-softmax update),
              "Striped Ring Attention", "Zigzag Ring Attention",
              "2. Sequence Parallelism".
+  [SP]       sourcepulse.org project summary of ring-flash-attention: the
+             "llama3" context-parallel variant.
   [AINEWS]   ainews.cool, ring-flash-attention long-context article,
              section "技术深度解析" (contiguous split, ring pass).
   [STRIPED]  briefgpt.xyz abstract of "Striped Attention: Faster Ring Attention
@@ -369,6 +371,32 @@ def ring_attention_sharded(q, k, v, layout, n_shards, scale, causal, cu_seqlens=
                 lse_l[bi, hi, rq] = l_acc
     return (unpermute(out_l, layout, N, axis=2, cu_seqlens=cu_seqlens),
             unpermute(lse_l[..., None], layout, N, axis=2, cu_seqlens=cu_seqlens)[..., 0])
+
+
+def llama3_rank_attention(q, k, v, rank, n_shards, scale, causal, cu_seqlens=None, do=None):
+    """One rank of the llama3 context-parallel form ([SP] "llama3" variant,
+    llama3_flash_attn_varlen_func): rank r holds the contiguous slice
+    [r*L, (r+1)*L) of the (packed) sequence, L = s / N, and its queries attend
+    to the all-gathered keys and values with the usual causal / per-sequence
+    mask.  Returns out (b, h, L, d), lse (b, h, L) of the slice and, when dO of
+    the slice is given, (dq of the slice, this rank's contributions to dk, dv of
+    the whole sequence): the gradient of L = sum(dO * out) restricted to the
+    slice's rows, i.e. the definition with dO = 0 outside the slice.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, h, s, d = q.shape
+    N = int(n_shards)
+    if N < 1 or s % N or not 0 <= rank < N:
+        raise ValueError("bad rank / n_shards")
+    L = s // N
+    rows = slice(rank * L, (rank + 1) * L)
+    out, lse = attention_fwd(q, k, v, scale, causal, cu_seqlens)
+    if do is None:
+        return out[:, :, rows], lse[:, :, rows]
+    do_full = np.zeros_like(q)
+    do_full[:, :, rows] = _f64(do)
+    dq, dk, dv = attention_bwd(q, k, v, do_full, scale, causal, cu_seqlens)
+    return out[:, :, rows], lse[:, :, rows], dq[:, :, rows], dk, dv
 
 
 def online_softmax_attention(q, k, v, scale, causal, kv_block=64, cu_seqlens=None):

@@ -419,6 +419,36 @@ def test_varlen_zigzag_sharded_then_merged_equals_full(n, causal):
     assert np.allclose(l, ref_l, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+@pytest.mark.parametrize("causal", [False, True])
+def test_llama3_ranks_compose_to_full_attention(n, causal):
+    """Outputs of the ranks concatenate to full varlen attention, and the ranks'
+    dk / dv contributions sum to the full gradient (the gradient is linear in dO)."""
+    lens = [5, 17, 0, 9, 29]
+    cu = cu_seqlens(lens)
+    s = cu[-1] + (-cu[-1]) % n
+    if s != cu[-1]:
+        lens[-1] += s - cu[-1]
+        cu = cu_seqlens(lens)
+    x = _inputs(1, 2, s, 8, 140 + n, with_do=True)
+    ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], 0.45, causal, cu_seqlens=cu)
+    ref_g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], 0.45, causal, cu_seqlens=cu)
+    L = s // n
+    dk_sum = np.zeros_like(ref_g[1])
+    dv_sum = np.zeros_like(ref_g[2])
+    for r in range(n):
+        rows = slice(r * L, (r + 1) * L)
+        o, l, dq, dk, dv = oracle.llama3_rank_attention(x["q"], x["k"], x["v"], r, n, 0.45, causal, cu_seqlens=cu,
+                                                        do=x["do"][:, :, rows])
+        assert np.allclose(o, ref_o[:, :, rows], atol=1e-12, rtol=0)
+        assert np.allclose(l, ref_l[:, :, rows], atol=1e-12, rtol=0)
+        assert np.allclose(dq, ref_g[0][:, :, rows], atol=1e-12, rtol=0)
+        dk_sum += dk
+        dv_sum += dv
+    assert np.allclose(dk_sum, ref_g[1], atol=1e-11, rtol=0)
+    assert np.allclose(dv_sum, ref_g[2], atol=1e-11, rtol=0)
+
+
 def test_pins_hold_on_the_unmodified_oracle():
     assert _pins_hold()
 
