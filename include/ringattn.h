@@ -18,6 +18,8 @@
  *             "2. 显存预分配" (caller-preallocated buffers).
  *   [AINEWS]  ainews.cool ring-flash-attention article, "技术深度解析".
  *   [STRIPED] briefgpt.xyz abstract of "Striped Attention" (causal imbalance).
+ *   [SP]      sourcepulse.org project summary of ring-flash-attention ("llama3"
+ *             context parallelism).
  *
  * Conventions shared by every call
  *   - Tensors are described by ra_tensor: a DEVICE pointer, a dtype, and up to
@@ -194,6 +196,30 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
                                const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t max_seqlen, int32_t layout,
                                int32_t n_shards, int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk,
                                ra_tensor* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* llama3 context-parallel form, one rank ([SP]: the "llama3" context
+ * parallelism variant, llama3_flash_attn_varlen_func): rank r of N holds the contiguous
+ * slice [r*L, (r+1)*L) of the packed buffer (L = total / N) and its queries
+ * attend to the all-gathered keys and values, with one cu_seqlens over the
+ * whole packed buffer.  q, out, dout, dq: (L, h, d) or (h, L, d), the rank's
+ * rows; k, v, dk, dv: (total, h, d) or (h, total, d); lse: (h, L) fp32.
+ * The forward gives the rank's out and lse (the rows of full varlen
+ * attention).  The backward gives dq of the rank's rows and the rank's
+ * contribution to dk and dv of every key: the gradient of sum(dO * out) over
+ * the rank's rows only (summing the N ranks' contributions gives the full
+ * gradient).  workspace: ring_attn_workspace_size(RA_OP_BWD, 1, h, L, d, 1)
+ * bytes.  Errors as for the varlen calls; rank outside [0, N) or total not a
+ * multiple of N is RA_ERR_INVALID_ARG. */
+ra_status ring_attn_llama3_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                                      const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                                      int32_t max_seqlen, int32_t rank, int32_t n_shards, int32_t causal,
+                                      float softmax_scale, ra_tensor* out, ra_tensor* lse, void* stream);
+ra_status ring_attn_llama3_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k,
+                                      const ra_tensor* v, const ra_tensor* out, const ra_tensor* lse,
+                                      const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                                      int32_t max_seqlen, int32_t rank, int32_t n_shards, int32_t causal,
+                                      float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* ring_attn_permute: original token order -> layout order along seq_dim:
  *   y[..., p, ...] = x[..., g(p), ...], g(p) = original token at layout position p.

@@ -22,7 +22,7 @@ __all__ = [
     "KERNELS", "RA_STATIC_SCRATCH_BYTES", "ring_attn_qkvpacked_fwd", "ring_attn_qkvpacked_bwd", "ring_attn_kvpacked_fwd",
     "ring_attn_kvpacked_bwd", "ring_attn_varlen_qkvpacked_fwd", "ring_attn_varlen_qkvpacked_bwd",
     "ring_attn_varlen_kvpacked_fwd", "ring_attn_varlen_kvpacked_bwd", "ring_attn_varlen_permute",
-    "ring_attn_varlen_unpermute",
+    "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_varlen_bwd", "ring_attn_permute", "ring_attn_unpermute", "ring_attn_workspace_size",
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
     "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch", "ring_attn_varlen_permute",
-    "ring_attn_varlen_unpermute",
+    "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd",
 )
 RA_STATIC_SCRATCH_BYTES = 16 << 20
 KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
@@ -81,6 +81,8 @@ def load():
         "ring_attn_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, P, SZ, P],
         "ring_attn_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
         "ring_attn_varlen_permute": [T, T, P, P, I32, I32, I32, I32, P],
+        "ring_attn_llama3_varlen_fwd": [T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, P],
+        "ring_attn_llama3_varlen_bwd": [T, T, T, T, T, T, P, P, I32, I32, I32, I32, I32, F32, T, T, T, P, SZ, P],
         "ring_attn_varlen_unpermute": [T, T, P, P, I32, I32, I32, I32, P],
         "ring_attn_permute": [T, T, I32, I32, I32, P],
         "ring_attn_unpermute": [T, T, I32, I32, I32, P],
@@ -293,6 +295,62 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
                                     ctypes.c_void_p(workspace.data_ptr()),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "ring_attn_varlen_bwd")
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------- llama3 form
+def _heads_of(x, rows):
+    return x.shape[1] if x.shape[0] == rows else x.shape[0]
+
+
+def ring_attn_llama3_varlen_fwd(q, k, v, cu_seqlens, rank, n_shards, causal=True, softmax_scale=None, max_seqlen=None,
+                                out=None, lse=None, stream=None):
+    """One rank of the llama3 form: q (L, h, d) or (h, L, d), the rank's contiguous slice of the
+    packed buffer (L = total / n_shards); k, v: all total rows.  Returns (out like q, lse (h, L))."""
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, q.device)
+    n = host.numel() - 1
+    total = int(host[-1])
+    if max_seqlen is None:
+        max_seqlen = int((host[1:] - host[:-1]).max())
+    L = total // int(n_shards)
+    h, d = _heads_of(q, L), q.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((h, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    t = [_t(x) for x in (q, k, v, out, lse)]
+    _check(lib.ring_attn_llama3_varlen_fwd(ctypes.byref(t[0]), ctypes.byref(t[1]), ctypes.byref(t[2]),
+                                           ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()), n,
+                                           int(max_seqlen), int(rank), int(n_shards), int(bool(causal)),
+                                           _scale(softmax_scale, d), ctypes.byref(t[3]), ctypes.byref(t[4]),
+                                           _stream(stream)), "ring_attn_llama3_varlen_fwd")
+    return out, lse
+
+
+def ring_attn_llama3_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, rank, n_shards, causal=True, softmax_scale=None,
+                                max_seqlen=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradient of one rank of the llama3 form: (dq of the rank's rows, the rank's contributions to dk, dv)."""
+    lib = load()
+    host, dev = _cu_pair(cu_seqlens, q.device)
+    n = host.numel() - 1
+    total = int(host[-1])
+    if max_seqlen is None:
+        max_seqlen = int((host[1:] - host[:-1]).max())
+    L = total // int(n_shards)
+    h, d = _heads_of(q, L), q.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, 1, h, L, d, 1)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    r = [ctypes.byref(x) for x in ts]
+    _check(lib.ring_attn_llama3_varlen_bwd(r[0], r[1], r[2], r[3], r[4], r[5], ctypes.c_void_p(dev.data_ptr()),
+                                           ctypes.c_void_p(host.data_ptr()), n, int(max_seqlen), int(rank),
+                                           int(n_shards), int(bool(causal)), _scale(softmax_scale, d), r[6], r[7],
+                                           r[8], ctypes.c_void_p(workspace.data_ptr()),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ring_attn_llama3_varlen_bwd")
     return dq, dk, dv
 
 

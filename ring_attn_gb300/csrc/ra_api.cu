@@ -197,15 +197,20 @@ struct TimedLaunch {
   } while (0)
 
 // Shared forward: fused ring (step < 0) or one ring step.
+// rank >= 0: one rank of the llama3 form: q and o hold that rank's L = S / N
+// rows (the contiguous slice [rank*L, (rank+1)*L)), k and v all S rows.
 ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout, int32_t n_shards, int32_t causal,
                      float scale, int32_t step, const Bhsd& o, int out_f32, float* lse, long long lsb, long long lsh,
-                     long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
-  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, o)) return RA_ERR_INVALID_ARG;
+                     long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1) {
+  if (!same_shape(k, v) || !same_shape(q, o)) return RA_ERR_INVALID_ARG;
+  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
+  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
+    return RA_ERR_INVALID_ARG;
   if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
-  RA_TRY(check_layout(layout, n_shards, q.s));
+  RA_TRY(check_layout(layout, n_shards, k.s));
   RA_TRY(check_scale(scale));
   if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
-  if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  if (k.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
   if (o.ss % (out_f32 ? 4 : 8) || o.sh % (out_f32 ? 4 : 8) || (o.b > 1 && o.sb % (out_f32 ? 4 : 8)))
     return RA_ERR_ALIGNMENT;
   FwdParams p;
@@ -213,8 +218,10 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   p.B = (int)q.b;
   p.H = (int)q.h;
   p.N = n_shards;
-  p.S = (int)q.s;
-  p.L = (int)(q.s / n_shards);
+  p.S = (int)k.s;
+  p.L = (int)(k.s / n_shards);
+  p.r_only = rank;
+  p.q_base = rank >= 0 ? rank * p.L : 0;
   p.layout = layout;
   p.causal = causal;
   p.step = step;
@@ -251,21 +258,28 @@ size_t bwd_ws_bytes(long long b, long long h, long long s, int n_shards) {
   return 2 * round256((size_t)b * h * n_shards * stat_rows_per_shard(s, n_shards) * sizeof(float));
 }
 
+// rank >= 0: one rank of the llama3 form: q, out, dout, dq hold that rank's
+// L = S / N rows, k, v, dk, dv all S rows (dk, dv get this rank's contribution),
+// and the statistics cover the rank's rows only.
 ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
                      const float* lse, long long lsb, long long lsh, long long lss, int32_t layout, int32_t n_shards,
                      int32_t causal, float scale, const Bhsd& dq, const Bhsd& dk, const Bhsd& dv, void* ws,
-                     size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
-  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, out) || !same_shape(q, dout) ||
-      !same_shape(q, dq) || !same_shape(q, dk) || !same_shape(q, dv))
+                     size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1) {
+  if (!same_shape(k, v) || !same_shape(k, dk) || !same_shape(k, dv) || !same_shape(q, out) ||
+      !same_shape(q, dout) || !same_shape(q, dq))
+    return RA_ERR_INVALID_ARG;
+  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
+  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
     return RA_ERR_INVALID_ARG;
   if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
-  RA_TRY(check_layout(layout, n_shards, q.s));
+  RA_TRY(check_layout(layout, n_shards, k.s));
   RA_TRY(check_scale(scale));
   if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
-  if (q.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, n_shards)) return RA_ERR_WORKSPACE;
-  const int stat_L = (int)stat_rows_per_shard(q.s, n_shards);
-  const size_t stats = round256((size_t)q.b * q.h * n_shards * stat_L * sizeof(float));
+  if (k.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  const int stat_N = rank >= 0 ? 1 : n_shards;  // shards whose rows the statistics hold
+  if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, stat_N)) return RA_ERR_WORKSPACE;
+  const int stat_L = (int)stat_rows_per_shard(q.s, stat_N);
+  const size_t stats = round256((size_t)q.b * q.h * stat_N * stat_L * sizeof(float));
   float* nD = static_cast<float*>(ws);
   float* nlse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + stats);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -278,12 +292,16 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.B = (int)q.b;
   p.H = (int)q.h;
   p.N = n_shards;
-  p.S = (int)q.s;
-  p.L = (int)(q.s / n_shards);
+  p.S = (int)k.s;
+  p.L = (int)(k.s / n_shards);
   p.layout = layout;
   p.causal = causal;
   p.n_qtiles = (p.L + kTileM - 1) / kTileM;
   p.n_ktiles = (p.L + kTileN - 1) / kTileN;
+  p.r_only = rank;
+  p.q_base = rank >= 0 ? rank * p.L : 0;
+  p.stat_N = stat_N;
+  p.stat_r0 = rank >= 0 ? rank : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.stat_L = stat_L;
@@ -311,7 +329,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, n_shards, stat_L, st)));
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, st)));
   }
   {
     TimedLaunch tl(RA_KERNEL_BWD, st);
@@ -594,6 +612,56 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,
                     stream);
+}
+
+// One rank of the llama3 form: shapes of the local (L rows) and full (total rows) tensors.
+static ra_status llama3_shapes(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs, int32_t max_seqlen,
+                               int32_t rank, int32_t n_shards, long long* total, long long* L) {
+  RA_TRY(check_cu(cu_dev, cu_host, n_seqs, max_seqlen, total));
+  if (n_shards < 1 || rank < 0 || rank >= n_shards || *total % n_shards) return RA_ERR_INVALID_ARG;
+  *L = *total / n_shards;
+  return RA_OK;
+}
+
+ra_status ring_attn_llama3_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
+                                      const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                                      int32_t max_seqlen, int32_t rank, int32_t n_shards, int32_t causal,
+                                      float softmax_scale, ra_tensor* out, ra_tensor* lse, void* stream) {
+  long long total = 0, L = 0;
+  RA_TRY(llama3_shapes(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, rank, n_shards, &total, &L));
+  Bhsd vq, vk, vv, vo;
+  RA_TRY(check_thd(q, L, &vq));
+  RA_TRY(check_thd(k, total, &vk));
+  RA_TRY(check_thd(v, total, &vv));
+  RA_TRY(check_thd(out, L, &vo));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, 1, vq.h, L, &lsb, &lsh, &lss));
+  return fwd_common(vq, vk, vv, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, vo, 0,
+                    static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream, rank);
+}
+
+ra_status ring_attn_llama3_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k,
+                                      const ra_tensor* v, const ra_tensor* out, const ra_tensor* lse,
+                                      const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
+                                      int32_t max_seqlen, int32_t rank, int32_t n_shards, int32_t causal,
+                                      float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  long long total = 0, L = 0;
+  RA_TRY(llama3_shapes(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, rank, n_shards, &total, &L));
+  Bhsd vdo, vq, vk, vv, vo, vdq, vdk, vdv;
+  RA_TRY(check_thd(dout, L, &vdo));
+  RA_TRY(check_thd(q, L, &vq));
+  RA_TRY(check_thd(k, total, &vk));
+  RA_TRY(check_thd(v, total, &vv));
+  RA_TRY(check_thd(out, L, &vo));
+  RA_TRY(check_thd(dq, L, &vdq));
+  RA_TRY(check_thd(dk, total, &vdk));
+  RA_TRY(check_thd(dv, total, &vdv));
+  long long lsb, lsh, lss;
+  RA_TRY(check_lse(lse, 1, vq.h, L, &lsb, &lsh, &lss));
+  return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, RA_LAYOUT_CONTIGUOUS,
+                    n_shards, causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,
+                    stream, rank);
 }
 
 static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t layout, int32_t n_shards,

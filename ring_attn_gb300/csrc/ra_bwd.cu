@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const long long stat_bh = ((long long)b * p.H + h) * p.N * p.stat_L;  // statistics row of (b, h, shard 0)
+  const long long stat_bh = ((long long)b * p.H + h) * p.stat_N * p.stat_L;  // statistics row of (b, h, first shard)
 
   if (warp < 4) {
     regs_dec<kDkdvRegsLow>();
@@ -193,10 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
         const int st = i & 1;
         const uint32_t par = ((i >> 1) - 1) & 1;
-        const int qrow = r * p.L + qt * kTileM;
+        const int qrow = r * p.L + qt * kTileM - p.q_base;
         if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) return false;
         // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
-        const long long e0 = stat_bh + (long long)r * p.stat_L + qt * kTileM;
+        const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
         mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.y / p.H, h = blockIdx.y % p.H;
   // causal: the later query tiles carry more work, start them first
   const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  const int r = x / p.n_qtiles;
+  const int r = p.r_only >= 0 ? p.r_only : x / p.n_qtiles;
   const int i0 = (x % p.n_qtiles) * kTileM;
   QRange qr;
   make_qrange(p, r, i0, kTileM, qr);
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
       const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
       if (is_k) {
-        const int qrow = r * p.L + i0;
+        const int qrow = r * p.L + i0 - p.q_base;
         mbar_expect_tx(BAR(F_QDO_FULL), 2 * LY::kTile);
         for (int c = 0; c < D / 64; ++c) {
           tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
     if (cu_of(p)) row_key_bounds(p, gq, rk_lo, rk_hi);
     // this row's statistics, negated (padding rows: -lse2 = -inf, -D = 0, so P = dS = 0)
-    const long long srow = (((long long)b * p.H + h) * p.N + r) * p.stat_L + i;
+    const long long srow = (((long long)b * p.H + h) * p.stat_N + (r - p.stat_r0)) * p.stat_L + i;
     const uint64_t nl2 = f32x2(__ldg(p.nlse2 + srow), __ldg(p.nlse2 + srow));
     const uint64_t nD2 = f32x2(__ldg(p.nD + srow), __ldg(p.nD + srow));
     const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     });
     // ---------------- epilogue: dQ = scale * (dS K), half the head dim per thread
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (long long)b * p.q_sb + (long long)h * p.q_sh +
-                         (long long)(r * p.L + i) * p.q_ss + half * (D / 2);
+                         (long long)(r * p.L + i - p.q_base) * p.q_ss + half * (D / 2);
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(F_DQ_DONE), 0, abort_flag, p.ctl, 63)) {
         tc_fence_after();
@@ -772,7 +772,7 @@ cudaError_t launch_bwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(ring_dq_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DqLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.N * p.n_qtiles), (unsigned)(p.B * p.H));
+    dim3 grid((unsigned)((p.r_only >= 0 ? 1 : p.N) * p.n_qtiles), (unsigned)(p.B * p.H));
     ring_dq_kernel<D, VL><<<grid, kThreads, DqLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);
   }
   return cudaGetLastError();

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // causal: the later query rows carry more work, start them first
   const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
-  const int r = x / n_pairs;
+  const int r = p.r_only >= 0 ? p.r_only : x / n_pairs;
   const int i0 = (x % n_pairs) * kRowsPerCta;
   QRange cta;  // both query tiles together: decides which key tiles are visited
   make_qrange(p, r, i0, kRowsPerCta, cta);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
       const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
       if (is_k && !(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
-        const int prow0 = r * p.L + i0;
+        const int prow0 = r * p.L + i0 - p.q_base;
         mbar_expect_tx(BAR(B_Q_FULL), kQTiles * LY::kTile);
         for (int t = 0; t < kQTiles; ++t)
           for (int c = 0; c < D / 64; ++c)
@@ -379,8 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     });
 
-    const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(r * p.L + i) * p.o_ss;
-    float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + (long long)(r * p.L + i) * p.l_ss;
+    const long long qpos = (long long)(r * p.L + i - p.q_base);  // row of q / out / lse
+    const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + qpos * p.o_ss;
+    float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + qpos * p.l_ss;
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(B_O_DONE), 0, abort_flag, p.ctl, 9)) {
         tc_fence_after();
@@ -448,7 +449,7 @@ cudaError_t launch_fwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   e = cudaFuncSetAttribute(ring_fwd_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
-  dim3 grid((unsigned)(p.N * n_pairs), (unsigned)(p.B * p.H));
+  dim3 grid((unsigned)((p.r_only >= 0 ? 1 : p.N) * n_pairs), (unsigned)(p.B * p.H));
   FwdParamsT<VL> pv;
   static_cast<FwdParams&>(pv) = p;
   ring_fwd_kernel<D, VL><<<grid, kThreads, LY::kAlloc, st>>>(tq, tk, tv, pv);

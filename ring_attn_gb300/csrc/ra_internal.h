@@ -25,6 +25,8 @@ struct FwdParams {
   long long l_sb, l_sh, l_ss;
   const int* cu;            // varlen cu_seqlens (device) or nullptr
   int n_seqs;
+  int q_base;               // token row of q / out / lse row 0 (one rank's slice: r_only * L, else 0)
+  int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
   DevCtl ctl;
 };
 
@@ -45,6 +47,9 @@ struct BwdParams {
   long long v_sb, v_sh, v_ss;   // strides of dv
   const int* cu;
   int n_seqs;
+  int q_base;               // token row of q / dO / out / dq row 0 (one rank's slice: r_only * L, else 0)
+  int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
+  int stat_N, stat_r0;      // the statistics hold shards [stat_r0, stat_r0 + stat_N)
   DevCtl ctl;
 };
 

@@ -256,12 +256,14 @@ __device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, 
   return !p.causal || token_of(p.layout, p.N, p.L, r, i0) >= k.gk_hi;
 }
 
-// Calls f(r, qt) for every query tile (QT rows) the keys of k serve, in ring order.
+// Calls f(r, qt) for every query tile (QT rows) the keys of k serve, in ring
+// order (only Q shard p.r_only when it is set).
 template <int QT, class P, class F>
 __device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nqt, F&& f) {
   for (int t = 0; t < p.N; ++t) {
     int r = k.s + t;
     if (r >= p.N) r -= p.N;
+    if (p.r_only >= 0 && r != p.r_only) continue;
     int lo, hi;
     q_range<QT>(p, k, r, nqt, lo, hi);
     for (int qt = lo; qt < hi; ++qt)

@@ -139,6 +139,22 @@ def test_varlen_rejects_bad_cu_seqlens(lib):
     assert call([0, 40, 64], 2, layout=2) == 2   # stripe varlen: not supported
 
 
+def test_llama3_rejects_bad_rank_and_shapes(lib):
+    k = _fake((64, 2, 64))
+    lse = _fake((2, 16), ra.RA_FP32)
+
+    def call(q, rank, n=4):
+        arr = (ctypes.c_int32 * 3)(0, 40, 64)
+        return lib.ring_attn_llama3_varlen_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k),
+                                               ctypes.c_void_p(0x1000), ctypes.cast(arr, ctypes.c_void_p), 2, 64,
+                                               rank, n, 1, 0.125, ctypes.byref(q), ctypes.byref(lse), None)
+
+    assert call(_fake((16, 2, 64)), 4) == 1        # rank outside [0, n_shards)
+    assert call(_fake((16, 2, 64)), -1) == 1
+    assert call(_fake((32, 2, 64)), 1) == 1        # q is not the rank's slice of total / n_shards rows
+    assert call(_fake((16, 2, 64)), 0, n=3) == 1   # 64 tokens do not split into 3 ranks
+
+
 def test_varlen_permute_rejects_bad_arguments(lib):
     x = _fake((64, 2, 64))
 

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from tests.helpers import (assert_close, assert_lse_close, check_no_device_error, f64, lse_to_original, to_layout,
+from tests.helpers import (TOL_MAX_ABS, assert_close, assert_lse_close, check_no_device_error, f64, lse_to_original, to_layout,
                            to_original)
 from workload import cu_seqlens, make_qkv
 
@@ -236,6 +236,53 @@ def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d):
     assert_lse_close("lse", back(lse, 1).unsqueeze(0), ref_l)
     for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref_g):
         assert_close(name, back(got).transpose(0, 1).unsqueeze(0), r)
+
+
+# ----------------------------------------------------------------------------- llama3 form
+@pytest.mark.parametrize("lens,n", [
+    ([100, 1, 300, 27, 84], 4),
+    ([700, 1300, 33, 2000, 15], 8),
+    ([256, 0, 128], 2),
+])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_llama3_varlen_ranks(ra, lens, n, causal, d):
+    """Every rank against the fp64 oracle; the ranks' dk / dv contributions sum
+    to the full varlen backward of the same inputs."""
+    h = 2
+    cu = cu_seqlens(lens)
+    total = cu[-1]
+    if total % n:
+        pytest.skip("total not divisible by n_shards")
+    L = total // n
+    x = make_qkv(1, h, total, d, 500 + len(lens) + n, with_do=True)
+    scale = d ** -0.5
+    g = {k: v[0].transpose(0, 1).contiguous().cuda() for k, v in x.items()}  # (total, h, d)
+    dk_sum = torch.zeros(total, h, d, dtype=torch.float64, device="cuda")
+    dv_sum = torch.zeros_like(dk_sum)
+    for r in range(n):
+        rows = slice(r * L, (r + 1) * L)
+        q_loc, do_loc = g["q"][rows].contiguous(), g["do"][rows].contiguous()
+        out, lse = ra.ring_attn_llama3_varlen_fwd(q_loc, g["k"], g["v"], cu, r, n, causal, scale)
+        dq, dk, dv = ra.ring_attn_llama3_varlen_bwd(do_loc, q_loc, g["k"], g["v"], out, lse, cu, r, n, causal, scale)
+        check_no_device_error(ra)
+        want = oracle.llama3_rank_attention(x["q"], x["k"], x["v"], r, n, scale, causal, cu_seqlens=cu,
+                                            do=x["do"][:, :, rows])
+        assert_close(f"out r{r}", out.transpose(0, 1).unsqueeze(0).cpu(), want[0])
+        assert_lse_close(f"lse r{r}", lse.unsqueeze(0).cpu(), want[1])
+        assert_close(f"dq r{r}", dq.transpose(0, 1).unsqueeze(0).cpu(), want[2])
+        assert_close(f"dk r{r}", dk.transpose(0, 1).unsqueeze(0).cpu(), want[3])
+        assert_close(f"dv r{r}", dv.transpose(0, 1).unsqueeze(0).cpu(), want[4])
+        dk_sum += dk.double()
+        dv_sum += dv.double()
+    out_f, lse_f = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, causal, scale)
+    _, dk_full, dv_full = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out_f, lse_f, cu, None, n, causal,
+                                                  scale)
+    # each of the n contributions was rounded to bf16 (up to half an ulp of its
+    # magnitude), so the max-abs bound grows with the number of ranks summed
+    bound = TOL_MAX_ABS * (1 + n / 4)
+    assert_close("sum dk", dk_sum.cpu(), dk_full.double().cpu(), max_abs=bound)
+    assert_close("sum dv", dv_sum.cpu(), dv_full.double().cpu(), max_abs=bound)
 
 
 # ----------------------------------------------------------------------------- bounded waits
