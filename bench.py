@@ -422,28 +422,53 @@ def main():
     if not (args.seq or args.heads):
         result["varlen"] = {k: _varlen_leg(ra, torch, k, peaks, dev) for k in (5, 6)}
 
-    # ---- e2e: host buffers in original order -> device -> permute -> fwd -> bwd -> unpermute -> host
+    # ---- e2e: host buffers in original order -> device -> permute -> fwd -> bwd -> unpermute -> host.
+    # Every step uploads its four inputs from pinned host memory and reads all
+    # five results back.  Uploads run on one copy stream and downloads on
+    # another, into double-buffered device staging, so the copies of one step
+    # overlap the compute of its neighbours (and dO's upload the forward).
     if not args.no_e2e:
         hin = {n: t.cpu().pin_memory() for n, t in x.items()}
         names_out = ("out", "dq", "dk", "dv")
         hout = {n: torch.empty_like(hin["q"]).pin_memory() for n in names_out}
         hlse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
-        dorig = {n: torch.empty_like(x["q"]) for n in x}
-        rorig = {n: torch.empty_like(x["q"]) for n in names_out}
-        lse_orig = torch.empty_like(lse)
+        dbuf = [{n: torch.empty_like(x["q"]) for n in x} for _ in range(2)]
+        rbuf = [{n: torch.empty_like(x["q"]) for n in names_out} for _ in range(2)]
+        lbuf = [torch.empty_like(lse) for _ in range(2)]
+        comp = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [{n: torch.cuda.Event() for n in x} for _ in range(2)]   # input n of buffer j uploaded
+        ev_used = [torch.cuda.Event() for _ in range(2)]                 # buffer j's inputs permuted
+        ev_out = [torch.cuda.Event() for _ in range(2)]                  # buffer j's results unpermuted
+        ev_read = [torch.cuda.Event() for _ in range(2)]                 # buffer j's results downloaded
 
-        def e2e_step():
-            for n in hin:
-                dorig[n].copy_(hin[n], non_blocking=True)
-                ra.ring_attn_permute(dorig[n], LAYOUT, N_SHARDS, out=g[n])
+        def e2e_step(i):
+            j = i % 2
+            up.wait_event(ev_used[j])
+            with torch.cuda.stream(up):
+                for n in ("q", "k", "v", "do"):
+                    dbuf[j][n].copy_(hin[n], non_blocking=True)
+                    ev_in[j][n].record(up)
+            for n in ("q", "k", "v", "do"):
+                comp.wait_event(ev_in[j][n])
+                ra.ring_attn_permute(dbuf[j][n], LAYOUT, N_SHARDS, out=g[n])
+            ev_used[j].record(comp)
             step()
+            comp.wait_event(ev_read[j])
             for n, src in zip(names_out, (out, dq, dk, dv)):
-                ra.ring_attn_unpermute(src, LAYOUT, N_SHARDS, out=rorig[n])
-                hout[n].copy_(rorig[n], non_blocking=True)
-            ra.ring_attn_unpermute(lse, LAYOUT, N_SHARDS, out=lse_orig)
-            hlse.copy_(lse_orig, non_blocking=True)
+                ra.ring_attn_unpermute(src, LAYOUT, N_SHARDS, out=rbuf[j][n])
+            ra.ring_attn_unpermute(lse, LAYOUT, N_SHARDS, out=lbuf[j])
+            ev_out[j].record(comp)
+            down.wait_event(ev_out[j])
+            with torch.cuda.stream(down):
+                for n in names_out:
+                    hout[n].copy_(rbuf[j][n], non_blocking=True)
+                hlse.copy_(lbuf[j], non_blocking=True)
+                ev_read[j].record(down)
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
+        comp.wait_stream(down)
         torch.cuda.synchronize()
         k_e2e = max(3, min(args.steps, 10))
         if dist is not None:
@@ -451,8 +476,10 @@ def main():
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record()
-        for _ in range(k_e2e):
-            e2e_step()
+        for i in range(k_e2e):
+            e2e_step(i)
+        comp.wait_stream(down)
+        comp.wait_stream(up)
         a1.record()
         torch.cuda.synchronize()
         e_ms = a0.elapsed_time(a1) / k_e2e
@@ -461,7 +488,9 @@ def main():
         d2h = sum(t.numel() * t.element_size() for t in hout.values()) + hlse.numel() * 4
         result["e2e"] = {"value": job_tflops(world, STEP_FLOP, e_ms), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-                         "steps": k_e2e, "path": "pinned host -> C-ABI permute, fwd, bwd, unpermute -> pinned host"}
+                         "steps": k_e2e,
+                         "path": "pinned host -> C-ABI permute, fwd, bwd, unpermute -> pinned host; uploads and "
+                                 "downloads on two copy streams, double-buffered, overlapping the compute"}
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if rank == 0 and world == 1 and not args.no_cpu:
