@@ -520,7 +520,9 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
   // when every row start allows it
   const bool v8 = d % 8 == 0 && 32 % (d / 8) == 0 && oa[0] % 8 == 0 && oa[1] % 8 == 0 && oa[2] % 8 == 0 &&
                   ob[0] % 8 == 0 && ob[1] % 8 == 0 && ob[2] % 8 == 0 && aligned(out_blk->data, 16);
-  a.vec = v8 ? 8 : 4;
+  // 16 columns (four 16-byte fp32 accesses, two 16-byte bf16 accesses) for a bf16 block
+  const bool v16 = v8 && !a.blk_f32 && d % 16 == 0 && 32 % (d / 16) == 0;
+  a.vec = v16 ? 16 : (v8 ? 8 : 4);
   a.qshift = 0;
   while ((1LL << a.qshift) < d / a.vec) ++a.qshift;
   TimedLaunch tl(RA_KERNEL_LSE_MERGE, static_cast<cudaStream_t>(stream));

@@ -103,7 +103,7 @@ struct MergeArgs {
   long long ob_s0, ob_s1, ob_s2;
   long long lb_s0, lb_s1, lb_s2;
   int flat;              // the three row dims collapse to one stride per tensor (the *_s2 strides)
-  int vec;               // columns per thread: 8, or 4 when the row layout does not allow 8
+  int vec;               // columns per thread: 16 or 8, or 4 when the row layout does not allow 8
   int qshift;            // log2(d / vec)
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st);

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vp
 
 // ------------------------------------------------------------------ LSE merge
 // A group of d/VEC threads (a power of two dividing 32, so a group sits inside
-// one warp) owns a row, VEC consecutive columns per thread:
+// one warp) owns a row, VEC (4, 8 or 16) consecutive columns per thread:
 //   lse_new = max(a, b) + log1p(exp(-|a - b|)),  w = exp(lse_blk - lse_new),
 //   out_acc += w * (out_blk - out_acc).
 // Each thread handles UNROLL rows per loop turn and issues every load before
@@ -104,13 +104,17 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
         for (int k = 0; k < NV; ++k)
           ob[u][k] = live[u] ? __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.out_blk) + bofs) + k)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      } else if (VEC == 8) {
-        const uint4 raw = live[u] ? __ldcs(reinterpret_cast<const uint4*>(
-                                        reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs))
-                                  : make_uint4(0u, 0u, 0u, 0u);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        ob[u][0] = make_float4(__low2float(h[0]), __high2float(h[0]), __low2float(h[1]), __high2float(h[1]));
-        ob[u][NV - 1] = make_float4(__low2float(h[2]), __high2float(h[2]), __low2float(h[3]), __high2float(h[3]));
+      } else if (VEC % 8 == 0) {
+#pragma unroll
+        for (int k8 = 0; k8 < VEC / 8; ++k8) {
+          const uint4 raw = live[u] ? __ldcs(reinterpret_cast<const uint4*>(
+                                          reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs) + k8)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          ob[u][2 * k8] = make_float4(__low2float(h[0]), __high2float(h[0]), __low2float(h[1]), __high2float(h[1]));
+          ob[u][2 * k8 + 1] =
+              make_float4(__low2float(h[2]), __high2float(h[2]), __low2float(h[3]), __high2float(h[3]));
+        }
       } else {
         const uint2 raw = live[u] ? __ldcs(reinterpret_cast<const uint2*>(
                                         reinterpret_cast<const __nv_bfloat16*>(a.out_blk) + bofs))
@@ -239,12 +243,16 @@ cudaError_t launch_permute(const PermuteArgs& a_in, cudaStream_t st) {
 
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
   const long long total = a.rows * (a.d / 4);
-  if (a.vec == 8) {
+  // two rows in flight per thread: measured faster than four on the benchmark
+  // shape (occupancy beats per-thread depth)
+  if (a.vec == 16) {
+    lse_merge_kernel<false, 16, 2><<<grid_for(a.rows * (a.d / 16), kThreads), kThreads, 0, st>>>(a);
+  } else if (a.vec == 8) {
     const long long items = a.rows * (a.d / 8);
     if (a.blk_f32)
       lse_merge_kernel<true, 8, 2><<<grid_for(items, kThreads), kThreads, 0, st>>>(a);
     else
-      lse_merge_kernel<false, 8, 4><<<grid_for(items, kThreads), kThreads, 0, st>>>(a);
+      lse_merge_kernel<false, 8, 2><<<grid_for(items, kThreads), kThreads, 0, st>>>(a);
   } else if (a.blk_f32) {
     lse_merge_kernel<true, 4, 2><<<grid_for(total, kThreads), kThreads, 0, st>>>(a);
   } else {
