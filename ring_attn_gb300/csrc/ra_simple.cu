@@ -18,36 +18,61 @@ int grid_for(long long work_items, int per_block) {
 
 // ------------------------------------------------------------------ permutation
 // A "row" is the packed run of elements after the sequence dimension, moved as
-// vpr vectors V (16 bytes when the row allows it).  A block handles
-// rows_per_block rows per turn, vpr threads per row, so the row's source and
-// destination are decoded once per thread and turn, not per element.
-template <typename V>
+// vpr vectors V (16 bytes when the row allows it).  blockIdx.y walks the outer
+// index (decoded once per block); blockIdx.x walks the layout positions with
+// rows_per_block rows per block and turn, vpr threads per row, so a row costs
+// its layout map and two multiply-adds.  When a row is one vector per thread,
+// each thread moves UNROLL rows per turn, all loads before the stores
+// (streaming cache hints: every byte is read and written once).
+template <typename V, int UNROLL>
 __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vpr, int rows_per_block) {
-  const long long total_rows = a.n_outer * a.s;
   const int rloc = threadIdx.x / vpr, v = threadIdx.x % vpr;
   if (rloc >= rows_per_block) return;
   const int L = a.s / a.N;
-  for (long long rp = (long long)blockIdx.x * rows_per_block + rloc; rp < total_rows;
-       rp += (long long)gridDim.x * rows_per_block) {
-    const int p = (int)(rp % a.s);           // layout position
-    long long o = rp / a.s;                  // outer index
+  const int pstride = (int)gridDim.x * rows_per_block;
+  for (long long o = blockIdx.y; o < a.n_outer; o += gridDim.y) {
     const long long o2 = o % a.outer_shape[2];
-    o /= a.outer_shape[2];
-    const long long o1 = o % a.outer_shape[1];
-    const long long o0 = o / a.outer_shape[1];
-    // original token at layout position p
-    const long long g = a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
-                        : a.layout == LAYOUT_ZIGZAG ? vz_token(a.cu, a.n_seqs, a.N, p / L, p % L)
-                                                    : p;
-    const long long src_pos = a.inverse ? p : g;
-    const long long dst_pos = a.inverse ? g : p;
-    const long long so = o0 * a.src_outer_stride[0] + o1 * a.src_outer_stride[1] + o2 * a.src_outer_stride[2] +
-                         src_pos * a.src_seq_stride;
-    const long long dof = o0 * a.dst_outer_stride[0] + o1 * a.dst_outer_stride[1] + o2 * a.dst_outer_stride[2] +
-                          dst_pos * a.dst_seq_stride;
-    const V* src = reinterpret_cast<const V*>(reinterpret_cast<const char*>(a.src) + so * a.esize);
-    V* dst = reinterpret_cast<V*>(reinterpret_cast<char*>(a.dst) + dof * a.esize);
-    for (int k = v; k < a.vpr_total; k += vpr) dst[k] = __ldg(src + k);
+    const long long o01 = o / a.outer_shape[2];
+    const long long o1 = o01 % a.outer_shape[1];
+    const long long o0 = o01 / a.outer_shape[1];
+    const char* sbase = reinterpret_cast<const char*>(a.src) +
+                        (o0 * a.src_outer_stride[0] + o1 * a.src_outer_stride[1] + o2 * a.src_outer_stride[2]) *
+                            a.esize;
+    char* dbase = reinterpret_cast<char*>(a.dst) +
+                  (o0 * a.dst_outer_stride[0] + o1 * a.dst_outer_stride[1] + o2 * a.dst_outer_stride[2]) * a.esize;
+    for (int p0 = (int)blockIdx.x * rows_per_block + rloc; p0 < a.s; p0 += UNROLL * pstride) {
+      const V* src[UNROLL];
+      V* dst[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int p = p0 + u * pstride;  // layout position
+        src[u] = nullptr;
+        dst[u] = nullptr;
+        if (p >= a.s) continue;
+        // original token at layout position p
+        const int g = a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
+                      : a.layout == LAYOUT_ZIGZAG ? vz_token(a.cu, a.n_seqs, a.N, p / L, p % L)
+                                                  : p;
+        const long long src_pos = a.inverse ? p : g;
+        const long long dst_pos = a.inverse ? g : p;
+        src[u] = reinterpret_cast<const V*>(sbase + src_pos * a.src_seq_stride * a.esize);
+        dst[u] = reinterpret_cast<V*>(dbase + dst_pos * a.dst_seq_stride * a.esize);
+      }
+      if (a.vpr_total == vpr) {
+        V val[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+          if (src[u]) val[u] = __ldcs(src[u] + v);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+          if (dst[u]) __stcs(dst[u] + v, val[u]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+          if (src[u])
+            for (int k = v; k < a.vpr_total; k += vpr) dst[u][k] = __ldg(src[u] + k);
+      }
+    }
   }
 }
 
@@ -216,6 +241,8 @@ int num_sms() {
   return cached[dev];
 }
 
+constexpr int kPermuteUnroll = 4;
+
 cudaError_t launch_permute(const PermuteArgs& a_in, cudaStream_t st) {
   PermuteArgs a = a_in;
   const long long row_bytes = a.inner * a.esize;
@@ -225,19 +252,25 @@ cudaError_t launch_permute(const PermuteArgs& a_in, cudaStream_t st) {
                      (a.src_outer_stride[1] * a.esize) % 16 == 0 && (a.src_outer_stride[2] * a.esize) % 16 == 0 &&
                      (a.dst_outer_stride[0] * a.esize) % 16 == 0 && (a.dst_outer_stride[1] * a.esize) % 16 == 0 &&
                      (a.dst_outer_stride[2] * a.esize) % 16 == 0;
-  const long long total_rows = a.n_outer * a.s;
   const long long vpr_total = vec16 ? row_bytes / 16 : a.inner;
   if (vpr_total > (1LL << 30)) return cudaErrorInvalidValue;
   a.vpr_total = (int)vpr_total;
   const int vpr = (int)(vpr_total < kThreads ? vpr_total : kThreads);  // threads per row
   const int rows_per_block = kThreads / vpr;
-  const int grid = grid_for(total_rows, rows_per_block);
+  // about 16 blocks per SM in total, split between the outer
+  // index (y) and the positions (x)
+  const long long gy = a.n_outer < 65535 ? a.n_outer : 65535;
+  long long gx = ((long long)num_sms() * 16 + gy - 1) / gy;
+  const long long need_x = (a.s + rows_per_block - 1) / rows_per_block;
+  if (gx > need_x) gx = need_x;
+  if (gx < 1) gx = 1;
+  const dim3 grid((unsigned)gx, (unsigned)gy);
   if (vec16)
-    permute_kernel<uint4><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
+    permute_kernel<uint4, kPermuteUnroll><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
   else if (a.esize == 4)
-    permute_kernel<uint32_t><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
+    permute_kernel<uint32_t, kPermuteUnroll><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
   else
-    permute_kernel<uint16_t><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
+    permute_kernel<uint16_t, kPermuteUnroll><<<grid, kThreads, 0, st>>>(a, vpr, rows_per_block);
   return cudaGetLastError();
 }
 
