@@ -183,46 +183,60 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
 // ------------------------------------------------------------------ backward pre / post
 // Per query row: -D = -sum_d dO * O and -lse2 = -lse * log2(e), stored per shard
 // with each shard's rows padded to stat_L (padding: -D = 0, -lse2 = -inf, so a
-// padded column contributes P = 0 and dS = 0).  d/8 threads per row (8 bf16 each).
+// padded column contributes P = 0 and dS = 0).  d/8 threads per row (8 bf16
+// each); blockIdx.y walks (b, h, shard), decoded once per block, and each
+// thread handles kPreUnroll rows per turn with every load issued first.
+constexpr int kPreUnroll = 4;
+
 __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* nD,
                                                             float* nlse2, int N, int stat_L) {
-  const int tpr = dout.d / 8;  // threads per row
+  const int tpr = dout.d / 8;  // threads per row; divides 32, so a row's threads share a warp
+  const int rows_per_block = kThreads / tpr;
+  const int rloc = threadIdx.x / tpr, part = threadIdx.x % tpr;
   const int L = dout.s / N;
-  const long long rows = (long long)dout.b * dout.h * N * stat_L;
-  const long long total = rows * tpr;
-  const long long step = (long long)gridDim.x * blockDim.x;
-  // tpr divides 32, so each row's threads sit in one warp and stay converged
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t - threadIdx.x % 32 < total; t += step) {
-    const bool live = t < total;
-    const long long row = live ? t / tpr : 0;  // (b, h, shard, padded local row)
-    const int part = (int)(t % tpr);
-    const int i = (int)(row % stat_L);
-    const long long bhr = row / stat_L;
+  const long long n_bhr = (long long)dout.b * dout.h * N;
+  const int istride = (int)gridDim.x * rows_per_block;
+  for (long long bhr = blockIdx.y; bhr < n_bhr; bhr += gridDim.y) {
     const int r = (int)(bhr % N);
     const long long bh = bhr / N;
     const long long h = bh % dout.h, b = bh / dout.h;
-    const bool real = live && i < L;
-    const long long p = (long long)r * L + i;  // layout position
-    float acc = 0.f;
-    if (real) {
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dout.data) +
-                                                           b * dout.sb + h * dout.sh + p * dout.ss) + part);
-      const uint4 y = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(out.data) +
-                                                           b * out.sb + h * out.sh + p * out.ss) + part);
-      const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x);
-      const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y);
+    const __nv_bfloat16* dsrc = reinterpret_cast<const __nv_bfloat16*>(dout.data) + b * dout.sb + h * dout.sh;
+    const __nv_bfloat16* osrc = reinterpret_cast<const __nv_bfloat16*>(out.data) + b * out.sb + h * out.sh;
+    const float* lsrc = lse.data + b * lse.sb + h * lse.sh;
+    // loop control follows the warp's first row, so every lane of a warp runs
+    // the same turns (the shuffle below needs them all)
+    const int wrow = rloc - rloc % (32 / tpr);
+    for (int t0 = (int)blockIdx.x * rows_per_block; t0 + wrow < stat_L; t0 += kPreUnroll * istride) {
+      const int i0 = t0 + rloc;
+      uint4 x[kPreUnroll], y[kPreUnroll];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 a = __bfloat1622float2(xv[u]);
-        const float2 c = __bfloat1622float2(yv[u]);
-        acc = fmaf(a.x, c.x, acc);
-        acc = fmaf(a.y, c.y, acc);
+      for (int u = 0; u < kPreUnroll; ++u) {
+        const int i = i0 + u * istride;
+        const bool real = i < L;
+        const long long p = (long long)r * L + i;  // layout position
+        x[u] = real ? __ldcs(reinterpret_cast<const uint4*>(dsrc + p * dout.ss) + part) : make_uint4(0, 0, 0, 0);
+        y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + p * out.ss) + part) : make_uint4(0, 0, 0, 0);
       }
-    }
-    for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && part == 0) {
-      nD[row] = -acc;
-      nlse2[row] = real ? lse.data[b * lse.sb + h * lse.sh + p * lse.ss] * -1.4426950408889634f : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kPreUnroll; ++u) {
+        const int i = i0 + u * istride;
+        const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+        const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 a2 = __bfloat1622float2(xv[k]);
+          const float2 c2 = __bfloat1622float2(yv[k]);
+          acc = fmaf(a2.x, c2.x, acc);
+          acc = fmaf(a2.y, c2.y, acc);
+        }
+        for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (part == 0 && i < stat_L) {
+          const long long row = bhr * stat_L + i;
+          nD[row] = -acc;
+          nlse2[row] = i < L ? lsrc[((long long)r * L + i) * lse.ss] * -1.4426950408889634f : -INFINITY;
+        }
+      }
     }
   }
 }
@@ -296,8 +310,14 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
 
 cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
                            int stat_L, cudaStream_t st) {
-  const long long total = (long long)dout.b * dout.h * N * stat_L * (dout.d / 8);
-  bwd_pre_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L);
+  const int rows_per_block = kThreads / (dout.d / 8);
+  const long long n_bhr = (long long)dout.b * dout.h * N;
+  const long long gy = n_bhr < 65535 ? n_bhr : 65535;
+  long long gx = ((long long)num_sms() * 16 + gy - 1) / gy;
+  const long long need_x = (stat_L + (long long)rows_per_block * kPreUnroll - 1) / ((long long)rows_per_block * kPreUnroll);
+  if (gx > need_x) gx = need_x;
+  if (gx < 1) gx = 1;
+  bwd_pre_kernel<<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L);
   return cudaGetLastError();
 }
 
