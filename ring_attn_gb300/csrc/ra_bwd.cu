@@ -759,18 +759,12 @@ cudaError_t launch_bwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   static_cast<BwdParams&>(pv) = p;
   if (which == 0) {
     // the register split inside the kernel is only safe with the launch allocation it was sized for
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, ring_dkdv_kernel<D, VL>);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kDkdvLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(ring_dkdv_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvLayout<D>::kAlloc);
+    cudaError_t e = configure_kernel<ring_dkdv_kernel<D, VL>>(kDkdvLaunchRegs, DkdvLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.N * p.n_ktiles), (unsigned)(p.B * p.H));
     ring_dkdv_kernel<D, VL><<<grid, kThreads, DkdvLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);
   } else {
-    cudaError_t e = cudaFuncSetAttribute(ring_dq_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqLayout<D>::kAlloc);
+    cudaError_t e = configure_kernel<ring_dq_kernel<D, VL>>(0, DqLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((p.r_only >= 0 ? 1 : p.N) * p.n_qtiles), (unsigned)(p.B * p.H));
     ring_dq_kernel<D, VL><<<grid, kThreads, DqLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);

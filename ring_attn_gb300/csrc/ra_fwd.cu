@@ -442,11 +442,7 @@ cudaError_t launch_fwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   using LY = FwdLayout<D>;
   // the register split inside the kernel is only safe with the launch
   // allocation it was sized for
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, ring_fwd_kernel<D, VL>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(ring_fwd_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kAlloc);
+  cudaError_t e = configure_kernel<ring_fwd_kernel<D, VL>>(kLaunchRegs, LY::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid((unsigned)((p.r_only >= 0 ? 1 : p.N) * n_pairs), (unsigned)(p.B * p.H));

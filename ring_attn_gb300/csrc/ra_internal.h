@@ -127,4 +127,33 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 
 int num_sms();
 
+// One-time set-up of a kernel on the current device, cached per kernel and
+// device: checks the compiled register count when the kernel's register split
+// depends on it (want_regs > 0) and raises its dynamic shared-memory limit.
+// Later calls on the device return the cached result without touching the driver.
+template <auto Kernel>
+cudaError_t configure_kernel(int want_regs, int smem_bytes) {
+  static int state[64] = {0};  // per device: 0 not yet, 1 ready, else the cudaError_t + 1000
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int s = __atomic_load_n(&state[dev], __ATOMIC_ACQUIRE);
+  if (s == 1) return cudaSuccess;
+  if (s > 1) return static_cast<cudaError_t>(s - 1000);
+  if (want_regs > 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, Kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != want_regs) {
+      __atomic_store_n(&state[dev], 1000 + (int)cudaErrorInvalidConfiguration, __ATOMIC_RELEASE);
+      return cudaErrorInvalidConfiguration;
+    }
+  }
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  __atomic_store_n(&state[dev], 1, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
+
 }  // namespace ra
