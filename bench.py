@@ -247,12 +247,19 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # per-kernel split, from a separate timed pass (the events sit between launches)
+    ra.ring_attn_timing_enable(True)
+    for _ in range(2):
+        step()
+    kt = {n: ra.ring_attn_timing_read(n) for n in ("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq")}
+    ra.ring_attn_timing_enable(False)
     st, info = ra.ring_attn_check_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st} info {info:#x} in the varlen leg")
     tf = 2.5 * w.fwd_flops() / (ms * 1e-3) / 1e12
     return {"workload": f"{w.name}: h{w.h} total {w.s} d{w.d}, {w.varlen_seqs} seqs, {w.n_shards} {w.layout} shards",
             "ms_per_step": ms, "tflops": tf, "frac_of_peak": tf / peaks["bf16_sustained"],
+            "kernel_ms": {n: t / max(c, 1) for n, (t, c) in kt.items()},
             "flop_convention": "fwd = sum_k 4*h*L_k^2*d/2; fwd+bwd = 2.5 x fwd"}
 
 

@@ -305,16 +305,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int j = k.j0 + jr;
     const bool valid_k = j < p.L;
-    const int gk = tok(p, k.s, valid_k ? j : k.j_last);
-    int rq_lo = 0, rq_hi = 0;  // varlen: the queries this key serves (see key_query_bounds)
-    if (cu_of(p)) key_query_bounds(p, gk, rq_lo, rq_hi);
+    // batched: tiles classified per key tile, masks per row on partial tiles;
+    // varlen: every key row's query window, set up once
+    RowWin win;
+    int gk = 0;
+    if constexpr (VL)
+      make_row_win(p, k.s, min(j, p.L - 1), true, win);
+    else
+      gk = tok(p, k.s, valid_k ? j : k.j_last);
     bool ok = true;
     int i = 0;
     walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
       const int st = i & 1;
       // padding query rows have -lse2 = -inf and -D = 0 (P = 0, dS = 0) without a mask
       int c_lo = 0, c_hi = kTileM;
-      if (!q_tile_full<kTileM>(p, k, r, qt)) key_query_window<kTileM>(p, valid_k, gk, rq_lo, rq_hi, r, qt, c_lo, c_hi);
+      if constexpr (VL) {
+        row_win_cols(p, win, r, qt * kTileM, kTileM, c_lo, c_hi);
+        if (!valid_k) c_lo = c_hi = 0;
+      } else if (!q_tile_full<kTileM>(p, k, r, qt)) {
+        key_query_window<kTileM>(p, valid_k, gk, r, qt, c_lo, c_hi);
+      }
       c_lo -= 64 * half;
       c_hi -= 64 * half;
       const bool masked = c_lo > 0 || c_hi < 64;
@@ -636,9 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int i = i0 + row;
     const bool valid = i < p.L;
-    const int gq = tok(p, r, valid ? i : max(qr.i_last, 0));
-    int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
-    if (cu_of(p)) row_key_bounds(p, gq, rk_lo, rk_hi);
+    // batched: tiles classified per query tile; varlen: every row's key window, set up once
+    RowWin win;
+    int gq = 0;
+    if constexpr (VL)
+      make_row_win(p, r, min(i, p.L - 1), false, win);
+    else
+      gq = tok(p, r, valid ? i : max(qr.i_last, 0));
     // this row's statistics, negated (padding rows: -lse2 = -inf, -D = 0, so P = dS = 0)
     const long long srow = (((long long)b * p.H + h) * p.stat_N + (r - p.stat_r0)) * p.stat_L + i;
     const uint64_t nl2 = f32x2(__ldg(p.nlse2 + srow), __ldg(p.nlse2 + srow));
@@ -671,7 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int j = 0;
     if (ok) walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int s, int kt) {
       int c_lo = 0, c_hi = kTileN;
-      if (!kv_tile_full(p, qr, s, kt)) row_key_window(p, gq, rk_lo, rk_hi, s, kt, c_lo, c_hi);
+      if constexpr (VL)
+        row_win_cols(p, win, s, kt * kTileN, kTileN, c_lo, c_hi);
+      else if (!kv_tile_full(p, qr, s, kt))
+        row_key_window(p, gq, s, kt, c_lo, c_hi);
       c_lo -= 64 * half;
       c_hi -= 64 * half;
       const bool masked = c_lo > 0 || c_hi < 64;

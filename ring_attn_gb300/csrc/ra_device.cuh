@@ -379,6 +379,42 @@ __device__ __forceinline__ int segment_of(const int* __restrict__ cu, int n_seqs
   return lo;
 }
 
+// segment_of for a target that is the same in every lane of a full warp,
+// with the answer known to be >= lo: the 32 lanes probe 32 evenly spaced
+// entries at a time, so each round of loads narrows the range 32-fold.
+__device__ __forceinline__ int segment_of_warp(const int* __restrict__ cu, int n_seqs, int t, int lo = 0) {
+  const int lane = threadIdx.x & 31;
+  int hi = n_seqs - 1;
+  while (lo < hi) {
+    const int step = (hi - lo + 32) >> 5;  // ceil((hi - lo + 1) / 32)
+    const int idx = lo + lane * step;
+    const bool le = idx <= hi && __ldg(cu + idx) <= t;
+    // lane 0 probes lo, where cu[lo] <= t holds already
+    const unsigned m = __ballot_sync(0xffffffffu, le) | 1u;
+    lo += (31 - __clz(m)) * step;
+    hi = min(hi, lo + step - 1);
+  }
+  return lo;
+}
+
+// segment_of for targets that do not decrease with the lane index, in a full
+// warp: two warp searches bound the lanes' segments, and a lane searches
+// between them only when the warp spans more than one sequence.
+__device__ __forceinline__ int segment_of_lanes(const int* __restrict__ cu, int n_seqs, int t) {
+  const int k0 = segment_of_warp(cu, n_seqs, __shfl_sync(0xffffffffu, t, 0));
+  const int t31 = __shfl_sync(0xffffffffu, t, 31);
+  if (t31 < __ldg(cu + k0 + 1)) return k0;
+  int lo = k0, hi = segment_of_warp(cu, n_seqs, t31, k0);
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
 // Zigzag varlen: sequence k (tokens [cu_k, cu_k1), a multiple of 2N) is cut
 // into 2N chunks of c = (cu_k1 - cu_k) / 2N tokens; every shard holds chunk r
 // then chunk 2N-1-r of each sequence in turn, so sequence k occupies local
@@ -392,6 +428,18 @@ __device__ __forceinline__ int vz_token_in(int cu_k, int cu_k1, int N, int r, in
 __device__ __forceinline__ int vz_token(const int* __restrict__ cu, int n_seqs, int N, int r, int i) {
   const int k = segment_of(cu, n_seqs, i * N);  // cu[k] / N <= i < cu[k+1] / N
   return vz_token_in(__ldg(cu + k), __ldg(cu + k + 1), N, r, i);
+}
+
+// One past the largest local index of shard s holding a token of a zigzag
+// sequence (local start base, chunk length c) whose offset in the sequence
+// is <= o; base when there is none.  Integer compares only: base and c are
+// computed once per sequence.
+__device__ __forceinline__ int vz_prefix_end(int base, int c, int N, int s, int o) {
+  if (o < s * c) return base;
+  if (o < (s + 1) * c) return base + (o - s * c) + 1;
+  if (o < (2 * N - 1 - s) * c) return base + c;
+  if (o < (2 * N - s) * c) return base + c + (o - (2 * N - 1 - s) * c) + 1;
+  return base + 2 * c;
 }
 
 // Largest local index of shard s holding a token of sequence k (tokens

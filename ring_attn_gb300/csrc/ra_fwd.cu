@@ -271,27 +271,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t tS = tl + LY::kTmemS + t * 128;
     const uint32_t tO = tl + LY::kTmemO + t * 128;
-    QRange qt;
-    make_qrange(p, r, i0 + t * kTileM, kTileM, qt);
     const int i = i0 + t * kTileM + row;
     const bool valid = i < p.L;
-    const int gq = tok(p, r, valid ? i : max(qt.i_last, 0));
-    int rk_lo = 0, rk_hi = 0;  // varlen: this row's key bounds (see row_key_bounds)
-    if (cu_of(p)) row_key_bounds(p, gq, rk_lo, rk_hi);
+    // batched: tiles classified per query tile, masks per row on partial tiles;
+    // varlen: every row's key window, set up once (padding rows take the last valid row's)
+    QRange qt;
+    RowWin win;
+    int gq = 0;
+    if constexpr (VL) {
+      make_row_win(p, r, min(i, p.L - 1), false, win);
+    } else {
+      make_qrange(p, r, i0 + t * kTileM, kTileM, qt);
+      gq = tok(p, r, valid ? i : max(qt.i_last, 0));
+    }
     float m_run = -INFINITY;  // running max, in log2 units (scores * scale * log2 e)
     float l_run = 0.f;        // running sum of exp2(x - m_run)
     bool ok = true;
     int j = 0;
     walk_tiles(p, cta, nkt, [&](int s, int kt) {
+      // column window [c_lo, c_hi) of allowed keys for this row (all 128 when the tile is full)
+      int c_lo = 0, c_hi = kTileN;
+      if constexpr (VL)
+        row_win_cols(p, win, s, kt * kTileN, kTileN, c_lo, c_hi);
+      else if (!kv_tile_full(p, qt, s, kt))
+        row_key_window(p, gq, s, kt, c_lo, c_hi);
+      const bool masked = c_lo > 0 || c_hi < kTileN;
       if (!wait_warp(BAR(B_S_FULL + t), j & 1, abort_flag, p.ctl, 7)) {
         ok = false;
         return false;
       }
       tc_fence_after();
-      // column window [c_lo, c_hi) of allowed keys for this row (all 128 when the tile is full)
-      int c_lo = 0, c_hi = kTileN;
-      if (!kv_tile_full(p, qt, s, kt)) row_key_window(p, gq, rk_lo, rk_hi, s, kt, c_lo, c_hi);
-      const bool masked = c_lo > 0 || c_hi < kTileN;
       // all 128 scores of the row in registers, in two halves: the row max of the
       // first half runs while the second half is loading
       uint32_t v[kTileN];

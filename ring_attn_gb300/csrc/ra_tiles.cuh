@@ -45,20 +45,41 @@ struct QRange {
   int seg_single;      // varlen: the segment of every valid row, or -1
 };
 
+// Searches of cu_seqlens: the first and last valid positions are the same in
+// every lane, and (varlen) every thread of the CTA calls this, so the
+// searches run warp-wide (segment_of_warp).
+template <class P>
+__device__ __forceinline__ void ends_and_segments(const P& p, int r, int ilo, int ihi, int& g_lo, int& g_hi, int& sa,
+                                                  int& sz) {
+  sa = sz = 0;
+  if (vz(p)) {
+    // local position i of any shard holds sequence k for cu[k] <= i N < cu[k+1]
+    sa = segment_of_warp(p.cu, p.n_seqs, ilo * p.N);
+    sz = segment_of_warp(p.cu, p.n_seqs, ihi * p.N, sa);
+    g_lo = vz_token_in(__ldg(p.cu + sa), __ldg(p.cu + sa + 1), p.N, r, ilo);
+    g_hi = vz_token_in(__ldg(p.cu + sz), __ldg(p.cu + sz + 1), p.N, r, ihi);
+    return;
+  }
+  g_lo = token_of(p.layout, p.N, p.L, r, ilo);
+  g_hi = token_of(p.layout, p.N, p.L, r, ihi);
+  if (cu_of(p)) {
+    sa = segment_of_warp(p.cu, p.n_seqs, g_lo);
+    sz = segment_of_warp(p.cu, p.n_seqs, g_hi, sa);
+  }
+}
+
 template <class P>
 __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows, QRange& q) {
   q.r = r;
   q.i0 = i0;
   q.i_last = min(i0 + rows, p.L) - 1;
   const int ilo = min(i0, p.L - 1);
-  q.gq_lo = tok(p, r, ilo);
-  q.gq_hi = tok(p, r, max(q.i_last, ilo));
+  int sa, sz;
+  ends_and_segments(p, r, ilo, max(q.i_last, ilo), q.gq_lo, q.gq_hi, sa, sz);
   q.key_lo = q.key_hi = 0;
   q.seg_lo = q.seg_hi = 0;
   q.seg_single = -1;
   if (cu_of(p)) {
-    const int sa = segment_of(p.cu, p.n_seqs, q.gq_lo);
-    const int sz = segment_of(p.cu, p.n_seqs, q.gq_hi);
     q.key_lo = __ldg(p.cu + sa);
     q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
     q.seg_lo = sa;
@@ -103,22 +124,13 @@ __device__ __forceinline__ void kv_range(const P& p, const QRange& q, int s, int
   hi = jm < 0 ? 0 : jm / kTileN + 1;
 }
 
-// True when every (valid row of q, key) pair of key tile kt of shard s is allowed.
+// True when every (valid row of q, key) pair of key tile kt of shard s is
+// allowed (batched calls; varlen rows use RowWin).
 template <class P>
 __device__ __forceinline__ bool kv_tile_full(const P& p, const QRange& q, int s, int kt) {
+  static_assert(!P::kVarlen, "varlen rows use RowWin");
   const int j0 = kt * kTileN;
   if (j0 + kTileN > p.L || q.i0 >= p.L) return false;
-  if (cu_of(p)) {
-    if (q.seg_single < 0) return false;
-    const int slo = __ldg(p.cu + q.seg_single), shi = __ldg(p.cu + q.seg_single + 1);
-    if (vz(p)) {
-      if (j0 < slo / p.N || j0 + kTileN > shi / p.N) return false;
-      return !p.causal || q.gq_lo >= vz_token_in(slo, shi, p.N, s, j0 + kTileN - 1);
-    }
-    const int base = s * p.L + j0;
-    if (base < slo || base + kTileN > shi) return false;
-    return !p.causal || q.gq_lo >= base + kTileN - 1;
-  }
   return !p.causal || q.gq_lo >= token_of(p.layout, p.N, p.L, s, j0 + kTileN - 1);
 }
 
@@ -135,38 +147,16 @@ __device__ __forceinline__ void walk_kv_tiles(const P& p, const QRange& q, int n
   }
 }
 
-// Per-row bounds for the varlen windows below: the row's key bounds in
-// tokens [rk_lo, rk_hi) for the contiguous layout (the causal bound folded
-// in), or its sequence [cu[k], cu[k+1]) for the zigzag layout.
+// Allowed key columns [c_lo, c_hi) of a query row (token gq) in key tile kt
+// of shard s (batched calls).
 template <class P>
-__device__ __forceinline__ void row_key_bounds(const P& p, int gq, int& rk_lo, int& rk_hi) {
-  const int sg = segment_of(p.cu, p.n_seqs, gq);
-  rk_lo = __ldg(p.cu + sg);
-  rk_hi = (p.causal && !vz(p)) ? gq + 1 : __ldg(p.cu + sg + 1);
-}
-
-// Allowed key columns [c_lo, c_hi) of a query row (token gq, varlen bounds
-// [rk_lo, rk_hi) from row_key_bounds) in key tile kt of shard s.
-template <class P>
-__device__ __forceinline__ void row_key_window(const P& p, int gq, int rk_lo, int rk_hi, int s, int kt, int& c_lo,
-                                               int& c_hi) {
+__device__ __forceinline__ void row_key_window(const P& p, int gq, int s, int kt, int& c_lo, int& c_hi) {
+  static_assert(!P::kVarlen, "varlen rows use RowWin");
   const int j0 = kt * kTileN;
   const int jlim = min(kTileN, p.L - j0);
   c_lo = 0;
   c_hi = jlim;
-  if (cu_of(p)) {
-    int lo, hi;  // allowed local keys [lo, hi) of shard s, relative to the tile
-    if (vz(p)) {
-      lo = rk_lo / p.N - j0;
-      hi = (p.causal ? vz_last_le(rk_lo, rk_hi, p.N, s, gq) + 1 : rk_hi / p.N) - j0;
-    } else {
-      const int base = s * p.L + j0;
-      lo = rk_lo - base;
-      hi = rk_hi - base;
-    }
-    c_lo = lo < 0 ? 0 : (lo > kTileN ? kTileN : lo);
-    c_hi = hi < 0 ? 0 : (hi > jlim ? jlim : hi);
-  } else if (p.causal) {
+  if (p.causal) {
     const int jm = last_local_at_or_before(p.layout, p.N, p.L, s, gq);
     c_hi = min(jlim, jm - j0 + 1);
   }
@@ -186,14 +176,12 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
   k.s = s;
   k.j0 = j0;
   k.j_last = min(j0 + kTileN, p.L) - 1;
-  k.gk_lo = tok(p, s, j0);
-  k.gk_hi = tok(p, s, k.j_last);
+  int sa, sz;
+  ends_and_segments(p, s, j0, k.j_last, k.gk_lo, k.gk_hi, sa, sz);
   k.qry_lo = k.qry_hi = 0;
   k.seg_lo = k.seg_hi = 0;
   k.seg_single = -1;
   if (cu_of(p)) {
-    const int sa = segment_of(p.cu, p.n_seqs, k.gk_lo);
-    const int sz = segment_of(p.cu, p.n_seqs, k.gk_hi);
     k.qry_lo = p.causal ? k.gk_lo : __ldg(p.cu + sa);
     k.qry_hi = __ldg(p.cu + sz + 1) - 1;
     k.seg_lo = sa;
@@ -237,22 +225,13 @@ __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int 
   lo = imin >= p.L ? nqt : imin / QT;
 }
 
-// True when every (key of k, valid query) pair of query tile qt (QT rows) of shard r is allowed.
+// True when every (key of k, valid query) pair of query tile qt (QT rows) of
+// shard r is allowed (batched calls; varlen rows use RowWin).
 template <int QT, class P>
 __device__ __forceinline__ bool q_tile_full(const P& p, const KRange& k, int r, int qt) {
+  static_assert(!P::kVarlen, "varlen rows use RowWin");
   const int i0 = qt * QT;
   if (i0 + QT > p.L || k.j0 + kTileN > p.L) return false;
-  if (cu_of(p)) {
-    if (k.seg_single < 0) return false;
-    const int slo = __ldg(p.cu + k.seg_single), shi = __ldg(p.cu + k.seg_single + 1);
-    if (vz(p)) {
-      if (i0 < slo / p.N || i0 + QT > shi / p.N) return false;
-      return !p.causal || vz_token_in(slo, shi, p.N, r, i0) >= k.gk_hi;
-    }
-    const int base = r * p.L + i0;
-    if (base < slo || base + QT > shi) return false;
-    return !p.causal || base >= k.gk_hi;
-  }
   return !p.causal || token_of(p.layout, p.N, p.L, r, i0) >= k.gk_hi;
 }
 
@@ -271,42 +250,82 @@ __device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nq
   }
 }
 
-// Per-key bounds for key_query_window: the queries a key serves in tokens
-// [rq_lo, rq_hi) for the contiguous layout (the causal bound folded in), or
-// its sequence [cu[k], cu[k+1]) for the zigzag layout.
-template <class P>
-__device__ __forceinline__ void key_query_bounds(const P& p, int gk, int& rq_lo, int& rq_hi) {
-  const int sg = segment_of(p.cu, p.n_seqs, gk);
-  rq_lo = (p.causal && !vz(p)) ? gk : __ldg(p.cu + sg);
-  rq_hi = __ldg(p.cu + sg + 1);
-}
-
-// Allowed query columns [c_lo, c_hi) of a key row (token gk, varlen bounds
-// [rq_lo, rq_hi) from key_query_bounds) in query tile qt (QT rows) of shard r.
+// Allowed query columns [c_lo, c_hi) of a key row (token gk) in query tile
+// qt (QT rows) of shard r (batched calls).
 template <int QT, class P>
-__device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int gk, int rq_lo, int rq_hi, int r, int qt,
-                                                 int& c_lo, int& c_hi) {
+__device__ __forceinline__ void key_query_window(const P& p, bool valid_k, int gk, int r, int qt, int& c_lo,
+                                                 int& c_hi) {
+  static_assert(!P::kVarlen, "varlen rows use RowWin");
   c_lo = c_hi = 0;
   if (!valid_k) return;
   const int i0 = qt * QT;
   const int ilim = min(QT, p.L - i0);
   c_hi = ilim;
-  if (cu_of(p)) {
-    int lo, hi;  // allowed local queries [lo, hi) of shard r, relative to the tile
-    if (vz(p)) {
-      lo = (p.causal ? vz_last_le(rq_lo, rq_hi, p.N, r, gk - 1) + 1 : rq_lo / p.N) - i0;
-      hi = rq_hi / p.N - i0;
-    } else {
-      const int base = r * p.L + i0;
-      lo = rq_lo - base;
-      hi = rq_hi - base;
-    }
-    c_lo = lo < 0 ? 0 : (lo > QT ? QT : lo);
-    c_hi = hi < 0 ? 0 : (hi > ilim ? ilim : hi);
-  } else if (p.causal) {
+  if (p.causal) {
     const int imin = last_local_at_or_before(p.layout, p.N, p.L, r, gk - 1) + 1;
     c_lo = max(0, imin - i0);
   }
+}
+
+// One varlen row's window: the local positions of a shard that the row may
+// meet (a query row: keys of its sequence at or before it; a key row: queries
+// of its sequence at or after it).  Set up once per row, with one warp-wide
+// search of cu_seqlens; per shard and tile only integer arithmetic follows.
+struct RowWin {
+  int a, b;         // contiguous: allowed tokens [a, b); zigzag: allowed offsets (a, b] in the sequence
+  int base, c;      // zigzag: the sequence's first local position (every shard) and its chunk length
+  int cur, lo, hi;  // shard `cur` allows local positions [lo, hi)
+};
+
+// Window of the row at local position i of shard r; returns its token.
+// Called by full warps with i not decreasing along the lanes (padding rows
+// pass the last valid position).  key_row: the dK/dV side.
+template <class P>
+__device__ __forceinline__ int make_row_win(const P& p, int r, int i, bool key_row, RowWin& w) {
+  static_assert(P::kVarlen, "batched rows use the tile classification");
+  int g, ck, ck1;
+  if (vz(p)) {
+    const int k = segment_of_lanes(p.cu, p.n_seqs, i * p.N);
+    ck = __ldg(p.cu + k);
+    ck1 = __ldg(p.cu + k + 1);
+    g = vz_token_in(ck, ck1, p.N, r, i);
+    const int o = g - ck, last = ck1 - ck - 1;
+    w.base = ck / p.N;
+    w.c = (ck1 - ck) / (2 * p.N);
+    w.a = key_row && p.causal ? o - 1 : -1;
+    w.b = !key_row && p.causal ? o : last;
+  } else {
+    g = r * p.L + i;
+    const int k = segment_of_lanes(p.cu, p.n_seqs, g);
+    ck = __ldg(p.cu + k);
+    ck1 = __ldg(p.cu + k + 1);
+    w.a = key_row && p.causal ? g : ck;
+    w.b = !key_row && p.causal ? g + 1 : ck1;
+    w.base = w.c = 0;
+  }
+  w.cur = -1;
+  w.lo = w.hi = 0;
+  return g;
+}
+
+// Allowed columns [c_lo, c_hi) of the row in the tile of `tlen` positions
+// starting at local position t0 of shard s.
+template <class P>
+__device__ __forceinline__ void row_win_cols(const P& p, RowWin& w, int s, int t0, int tlen, int& c_lo, int& c_hi) {
+  if (s != w.cur) {
+    w.cur = s;
+    if (vz(p)) {
+      w.lo = vz_prefix_end(w.base, w.c, p.N, s, w.a);
+      w.hi = vz_prefix_end(w.base, w.c, p.N, s, w.b);
+    } else {
+      w.lo = w.a - s * p.L;
+      w.hi = w.b - s * p.L;
+    }
+  }
+  const int lim = min(tlen, p.L - t0);
+  const int lo = w.lo - t0, hi = w.hi - t0;
+  c_lo = lo < 0 ? 0 : (lo > tlen ? tlen : lo);
+  c_hi = hi < 0 ? 0 : (hi > lim ? lim : hi);
 }
 
 }  // namespace ra
