@@ -442,19 +442,6 @@ __device__ __forceinline__ int vz_prefix_end(int base, int c, int N, int s, int 
   return base + 2 * c;
 }
 
-// Largest local index of shard s holding a token of sequence k (tokens
-// [cu_k, cu_k1)) that is <= g, or cu_k / N - 1 when there is none.
-__device__ __forceinline__ int vz_last_le(int cu_k, int cu_k1, int N, int s, int g) {
-  const int c = (cu_k1 - cu_k) / (2 * N);
-  const int base = cu_k / N;
-  const int o = g - cu_k;
-  if (o < s * c) return base - 1;
-  if (o < (s + 1) * c) return base + (o - s * c);
-  if (o < (2 * N - 1 - s) * c) return base + c - 1;
-  if (o < (2 * N - s) * c) return base + c + (o - (2 * N - 1 - s) * c);
-  return base + 2 * c - 1;
-}
-
 }  // namespace ra
 
 namespace ra {

@@ -40,9 +40,11 @@ __device__ __forceinline__ int tok(const P& p, int r, int i) {
 struct QRange {
   int r, i0, i_last;
   int gq_lo, gq_hi;    // original token indices of the first / last valid row
-  int key_lo, key_hi;  // contiguous varlen: keys any row may see (inclusive)
-  int seg_lo, seg_hi;  // varlen: segments of the first / last valid row
-  int seg_single;      // varlen: the segment of every valid row, or -1
+  // varlen: the keys any row may see.  Contiguous: tokens [key_lo, key_hi].
+  // Zigzag: local positions from key_lo in every shard up to, when causal, the
+  // last row's offset zo in its sequence (first local position zb, chunk zc),
+  // else up to key_hi.  Set once per CTA, so kv_range is integer compares.
+  int key_lo, key_hi, zb, zc, zo;
 };
 
 // Searches of cu_seqlens: the first and last valid positions are the same in
@@ -76,15 +78,17 @@ __device__ __forceinline__ void make_qrange(const P& p, int r, int i0, int rows,
   const int ilo = min(i0, p.L - 1);
   int sa, sz;
   ends_and_segments(p, r, ilo, max(q.i_last, ilo), q.gq_lo, q.gq_hi, sa, sz);
-  q.key_lo = q.key_hi = 0;
-  q.seg_lo = q.seg_hi = 0;
-  q.seg_single = -1;
-  if (cu_of(p)) {
+  q.key_lo = q.key_hi = q.zb = q.zc = q.zo = 0;
+  if (vz(p)) {
+    const int cz = __ldg(p.cu + sz), cz1 = __ldg(p.cu + sz + 1);
+    q.key_lo = __ldg(p.cu + sa) / p.N;
+    q.key_hi = cz1 / p.N - 1;
+    q.zb = cz / p.N;
+    q.zc = (cz1 - cz) / (2 * p.N);
+    q.zo = q.gq_hi - cz;
+  } else if (cu_of(p)) {
     q.key_lo = __ldg(p.cu + sa);
     q.key_hi = p.causal ? q.gq_hi : __ldg(p.cu + sz + 1) - 1;
-    q.seg_lo = sa;
-    q.seg_hi = sz;
-    q.seg_single = sa == sz ? sa : -1;
   }
 }
 
@@ -95,9 +99,8 @@ __device__ __forceinline__ void kv_range(const P& p, const QRange& q, int s, int
     int jlo, jhi;  // local key positions of shard s, inclusive
     if (vz(p)) {
       // keys of the rows' sequences up to the last row's token (local order is token order)
-      const int ca = __ldg(p.cu + q.seg_lo), cz = __ldg(p.cu + q.seg_hi), cz1 = __ldg(p.cu + q.seg_hi + 1);
-      jlo = ca / p.N;
-      jhi = p.causal ? vz_last_le(cz, cz1, p.N, s, q.gq_hi) : cz1 / p.N - 1;
+      jlo = q.key_lo;
+      jhi = p.causal ? vz_prefix_end(q.zb, q.zc, p.N, s, q.zo) - 1 : q.key_hi;
     } else {
       const int base = s * p.L;
       jlo = q.key_lo - base;
@@ -166,9 +169,11 @@ __device__ __forceinline__ void row_key_window(const P& p, int gq, int s, int kt
 struct KRange {
   int s, j0, j_last;
   int gk_lo, gk_hi;
-  int qry_lo, qry_hi;  // contiguous varlen: queries any key of the tile may serve (inclusive)
-  int seg_lo, seg_hi;  // varlen: segments of the first / last valid key
-  int seg_single;
+  // varlen: the queries any key may serve.  Contiguous: tokens [qry_lo, qry_hi].
+  // Zigzag: local positions up to qry_hi in every shard, from (causal) the
+  // first local position past offset zo of the first key's sequence (first
+  // local position zb, chunk zc), else from qry_lo.
+  int qry_lo, qry_hi, zb, zc, zo;
 };
 
 template <class P>
@@ -178,15 +183,17 @@ __device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k
   k.j_last = min(j0 + kTileN, p.L) - 1;
   int sa, sz;
   ends_and_segments(p, s, j0, k.j_last, k.gk_lo, k.gk_hi, sa, sz);
-  k.qry_lo = k.qry_hi = 0;
-  k.seg_lo = k.seg_hi = 0;
-  k.seg_single = -1;
-  if (cu_of(p)) {
+  k.qry_lo = k.qry_hi = k.zb = k.zc = k.zo = 0;
+  if (vz(p)) {
+    const int ca = __ldg(p.cu + sa), ca1 = __ldg(p.cu + sa + 1);
+    k.qry_lo = ca / p.N;
+    k.qry_hi = __ldg(p.cu + sz + 1) / p.N - 1;
+    k.zb = ca / p.N;
+    k.zc = (ca1 - ca) / (2 * p.N);
+    k.zo = k.gk_lo - 1 - ca;
+  } else if (cu_of(p)) {
     k.qry_lo = p.causal ? k.gk_lo : __ldg(p.cu + sa);
     k.qry_hi = __ldg(p.cu + sz + 1) - 1;
-    k.seg_lo = sa;
-    k.seg_hi = sz;
-    k.seg_single = sa == sz ? sa : -1;
   }
 }
 
@@ -197,9 +204,8 @@ __device__ __forceinline__ void q_range(const P& p, const KRange& k, int r, int 
     int ilo, ihi;  // local query positions of shard r, inclusive
     if (vz(p)) {
       // queries of the keys' sequences from the first key's token on
-      const int ca = __ldg(p.cu + k.seg_lo), ca1 = __ldg(p.cu + k.seg_lo + 1);
-      ilo = p.causal ? vz_last_le(ca, ca1, p.N, r, k.gk_lo - 1) + 1 : ca / p.N;
-      ihi = __ldg(p.cu + k.seg_hi + 1) / p.N - 1;
+      ilo = p.causal ? vz_prefix_end(k.zb, k.zc, p.N, r, k.zo) : k.qry_lo;
+      ihi = k.qry_hi;
     } else {
       const int base = r * p.L;
       ilo = k.qry_lo - base;
