@@ -44,26 +44,42 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
 }
 
-// One bf16 output row segment of N32 * 32 columns from TMEM, times mul.
+// The warp's 32 output row segments (lane l: N32 * 32 columns of row l, from
+// TMEM, times mul, as bf16) leave through a shared-memory slot of 32 * N32 * 64
+// bytes: each lane writes its segment there (16-byte pieces, the piece index
+// XOR the row's low bits, so the lanes spread over the banks), then the warp
+// stores whole segments with consecutive lanes on consecutive pieces.  Rows
+// [0, nvalid) are written; dst0 is row 0's segment, stride the row pitch.
 template <int N32>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, bool valid, __nv_bfloat16* dst) {
+__device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul, uint8_t* slot, __nv_bfloat16* dst0,
+                                                long long stride, int nvalid) {
+  constexpr int kPieces = 4 * N32;                      // 16-byte pieces per segment
+  constexpr int kSwz = kPieces < 8 ? kPieces - 1 : 7;  // XOR mask on the piece index
+  const int lane = threadIdx.x & 31;
+  uint8_t* mine = slot + lane * kPieces * 16;
 #pragma unroll
   for (int c = 0; c < N32; ++c) {
     uint32_t o[32];
     tmem_ld32(taddr + c * 32, o);
     tmem_ld_wait(o);
-    if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * mul, __uint_as_float(o[8 * u + 1]) * mul);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * mul, __uint_as_float(o[8 * u + 3]) * mul);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * mul, __uint_as_float(o[8 * u + 5]) * mul);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * mul, __uint_as_float(o[8 * u + 7]) * mul);
-        d4[u] = w;
-      }
+    for (int u = 0; u < 4; ++u) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * mul, __uint_as_float(o[8 * u + 1]) * mul);
+      w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * mul, __uint_as_float(o[8 * u + 3]) * mul);
+      w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * mul, __uint_as_float(o[8 * u + 5]) * mul);
+      w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * mul, __uint_as_float(o[8 * u + 7]) * mul);
+      *reinterpret_cast<uint4*>(mine + (((c * 4 + u) ^ (lane & kSwz)) << 4)) = w;
     }
+  }
+  __syncwarp();
+  constexpr int kRowsPer = 32 / kPieces;  // segments per warp-wide store
+  const int pc = lane % kPieces;
+#pragma unroll 1
+  for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
+    const int row = r0 + lane / kPieces;
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + row * kPieces * 16 + ((pc ^ (row & kSwz)) << 4));
+    if (row < nvalid) *reinterpret_cast<uint4*>(dst0 + row * stride + pc * 8) = v;
   }
 }
 
@@ -93,6 +109,7 @@ struct DkdvLayout {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDV = 256, kTmemDK = 256 + D;
+  static_assert(8 * 32 * D * 2 <= kStats, "output row slots exceed the operand buffers");
 };
 
 // Register split of the dK / dV kernel: the control warpgroup (TMA, MMA, TMEM)
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++i;
       return true;
     });
-    // ---------------- epilogue: warpgroup 1 writes the dV row, warpgroup 2 the dK row
+    // ---------------- epilogue: warpgroup 1 writes the dV rows, warpgroup 2 the dK rows
     const long long prow = (long long)k.s * p.L + j;
     __nv_bfloat16* dst = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
                                          (long long)h * p.v_sh + prow * p.v_ss
@@ -419,8 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(E_KV_DONE), 0, abort_flag, p.ctl, 38)) {
         tc_fence_after();
-        store_row_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale, valid_k,
-                               dst);
+        // every MMA is done: the operand buffers hold the warps' row slots
+        fence_proxy_async_smem();
+        const int j_w = j - lane;  // the warp's first key row
+        const long long pitch = half == 0 ? p.v_ss : p.k_ss;
+        store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
+                                sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch,
+                                min(max(p.L - j_w, 0), 32));
       }
     } else if (valid_k) {
       for (int u = 0; u < D / 8; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
@@ -460,6 +482,7 @@ struct DqLayout {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemQ = 256, kTmemDO = 256 + D / 2, kTmemDQ = 384;
+  static_assert(8 * 32 * D <= kBar, "output row slots exceed the operand buffers");
 };
 
 enum DqBar {
@@ -754,7 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(F_DQ_DONE), 0, abort_flag, p.ctl, 63)) {
         tc_fence_after();
-        store_row_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, valid, dst);
+        // every MMA is done: the operand buffers hold the warps' row slots
+        fence_proxy_async_smem();
+        const int i_w = i - lane;  // the warp's first query row
+        store_rows_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, sp + (warp - 4) * (32 * D),
+                                dst - lane * p.q_ss, p.q_ss, min(max(p.L - i_w, 0), 32));
       }
     } else if (valid) {
       for (int u = 0; u < D / 16; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
