@@ -377,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[4 * c4 + 3] = __float_as_uint(fast_exp2(x3));
       }
       if (masked) {
+        const uint64_t mw = bit_window64(c_lo, c_hi);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : 0u;
+        for (int c = 0; c < 64; ++c) v[c] = ((mw >> c) & 1ull) ? v[c] : 0u;
       }
       if (!wait_warp(BAR(E_DP_FULL), i & 1, abort_flag, p.ctl, 37)) {
         ok = false;
@@ -735,8 +736,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[c + 1] = __float_as_uint(fast_exp2(x1));
       }
       if (masked) {
+        const uint64_t mw = bit_window64(c_lo, c_hi);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) v[c] = (c >= c_lo && c < c_hi) ? v[c] : 0u;
+        for (int c = 0; c < 64; ++c) v[c] = ((mw >> c) & 1ull) ? v[c] : 0u;
       }
       if (!wait_warp(BAR(F_DP_FULL), j & 1, abort_flag, p.ctl, 62)) {
         ok = false;

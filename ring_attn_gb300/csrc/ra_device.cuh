@@ -326,6 +326,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Bits [lo, hi) of a 64-bit word (lo and hi clamped to [0, 64]; none when
+// lo >= hi): a row's allowed columns of a 64-column half tile, so masking a
+// column is one bit test and one select.
+__device__ __forceinline__ uint64_t bit_window64(int lo, int hi) {
+  lo = min(max(lo, 0), 64);
+  hi = min(max(hi, 0), 64);
+  const uint64_t below_hi = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+  const uint64_t below_lo = lo >= 64 ? ~0ull : ((1ull << lo) - 1ull);
+  return below_hi & ~below_lo;
+}
+
 // ------------------------------------------------------------------ layouts
 // Original token index of local position i in shard r (L tokens per shard).
 // 32-bit: the host validates s <= 2^30, so every token index fits.

@@ -320,9 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 96));
         }
         if (masked) {
+          const uint64_t mw = bit_window64(c_lo - 64 * hh, c_hi - 64 * hh);
 #pragma unroll
-          for (int c = 64 * hh; c < 64 * hh + 64; ++c)
-            v[c] = (c >= c_lo && c < c_hi) ? v[c] : __float_as_uint(-INFINITY);
+          for (int u = 0; u < 64; ++u)
+            v[64 * hh + u] = ((mw >> u) & 1ull) ? v[64 * hh + u] : __float_as_uint(-INFINITY);
         }
         // four chains of three-input maxima over the 64 scores of this half
 #pragma unroll
@@ -395,50 +396,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(B_O_DONE), 0, abort_flag, p.ctl, 9)) {
         tc_fence_after();
-        fence_proxy_async_smem();
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        // O leaves through shared memory (every MMA is done, so the operand
-        // buffers are free): each thread writes its row into its warp's slot
-        // (16-byte pieces, the piece index XOR the row's low bits, so the 32
-        // lanes spread over the banks), then the warp stores whole rows with
-        // consecutive lanes on consecutive pieces of a row.
-        const int esz = p.out_f32 ? 4 : 2;
-        const int nch = D * esz / 16;  // 16-byte pieces per row: 8, 16 or 32
-        uint8_t* slot = sp + (warp - 4) * (32 * D * 4);
-        uint8_t* mine = slot + lane * nch * 16;
+        if constexpr (!VL) {
+          // long CTAs: one row per thread, straight to global memory
+          const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + qpos * p.o_ss;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-          if (p.out_f32) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+            if (valid) {
+              if (p.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow + c * 32);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<float4*>(mine + (((c * 8 + k) ^ (lane & 7)) << 4)) =
-                  make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                              __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
-          } else {
+                for (int k = 0; k < 8; ++k)
+                  dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                       __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow + c * 32);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(mine + (((c * 4 + k) ^ (lane & 7)) << 4)) = v;
+                for (int k = 0; k < 4; ++k) {
+                  uint4 v;
+                  v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+                  v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+                  v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+                  v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+                  dst[k] = v;
+                }
+              }
             }
           }
-        }
-        __syncwarp();
-        const int rows_per = 32 / nch, lr = lane / nch, pc = lane % nch;
-        const int i_w = i0 + t * kTileM + (warp & 3) * 32;  // local position of the warp's first row
-        for (int R0 = 0; R0 < 32; R0 += rows_per) {
-          const int R = R0 + lr;
-          const uint4 val = *reinterpret_cast<const uint4*>(slot + R * nch * 16 + ((pc ^ (R & 7)) << 4));
-          if (i_w + R < p.L) {
-            const long long q_row = (long long)(r * p.L + i_w + R - p.q_base);
-            const long long e = (long long)b * p.o_sb + (long long)h * p.o_sh + q_row * p.o_ss;
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) + e * esz + pc * 16) = val;
+        } else {
+          fence_proxy_async_smem();
+          // varlen (short CTAs, where the epilogue weighs): O leaves through
+          // shared memory (every MMA is done, so the operand buffers are
+          // free).  Each thread writes its row into its warp's slot (16-byte
+          // pieces, the piece index XOR the row's low bits, so the 32 lanes
+          // spread over the banks), then the warp stores whole rows with
+          // consecutive lanes on consecutive pieces of a row.
+          const int esz = p.out_f32 ? 4 : 2;
+          const int nch = D * esz / 16;  // 16-byte pieces per row: 8, 16 or 32
+          uint8_t* slot = sp + (warp - 4) * (32 * D * 4);
+          uint8_t* mine = slot + lane * nch * 16;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+            if (p.out_f32) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4*>(mine + (((c * 8 + k) ^ (lane & 7)) << 4)) =
+                    make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(mine + (((c * 4 + k) ^ (lane & 7)) << 4)) = v;
+              }
+            }
+          }
+          __syncwarp();
+          const int rows_per = 32 / nch, lr = lane / nch, pc = lane % nch;
+          const int i_w = i0 + t * kTileM + (warp & 3) * 32;  // local position of the warp's first row
+          for (int R0 = 0; R0 < 32; R0 += rows_per) {
+            const int R = R0 + lr;
+            const uint4 val = *reinterpret_cast<const uint4*>(slot + R * nch * 16 + ((pc ^ (R & 7)) << 4));
+            if (i_w + R < p.L) {
+              const long long q_row = (long long)(r * p.L + i_w + R - p.q_base);
+              const long long e = (long long)b * p.o_sb + (long long)h * p.o_sh + q_row * p.o_ss;
+              *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) + e * esz + pc * 16) = val;
+            }
           }
         }
         if (valid) *lse_ptr = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
