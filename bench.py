@@ -42,7 +42,7 @@ STEP_FLOP = 2.5 * FWD_FLOP                         # fwd+bwd, 2.5x convention
 STEP_FLOP_ALG = 3.5 * FWD_FLOP                     # fwd + bwd (5 GEMMs vs 2)
 BWD_FLOP = 2.5 * FWD_FLOP                          # backward alone: 10*d per unmasked pair
 CPU_SAMPLE_TOKENS = 8192       # reference arm: one step of CPU work
-CPU_BASELINE_TOKENS = 16384    # cpu_baseline: ~10-30 s of CPU work
+CPU_BASELINE_TOKENS = 24576    # cpu_baseline: ~10-30 s of CPU work (about 12 s on 16 Arm cores)
 
 
 def _peaks():

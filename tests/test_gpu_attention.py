@@ -189,6 +189,7 @@ def test_varlen_fwd_bwd(ra, lens, n, causal, packed):
     ([4, 132, 260, 0, 508], 2),
     ([128, 24, 320, 8], 4),
     ([6 * 20, 6 * 7, 6 * 50], 3),
+    ([0, 4, 0, 8] * 300, 2),
 ])
 def test_varlen_zigzag_permute_bit_exact(ra, lens, n):
     cu = cu_seqlens(lens)
@@ -231,6 +232,44 @@ def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d):
 
     def back(t, seq_dim=0):
         return ra.ring_attn_varlen_unpermute(t.contiguous(), cu, "zigzag", n, seq_dim=seq_dim).cpu()
+
+    assert_close("out", back(out).transpose(0, 1).unsqueeze(0), ref_o)
+    assert_lse_close("lse", back(lse, 1).unsqueeze(0), ref_l)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref_g):
+        assert_close(name, back(got).transpose(0, 1).unsqueeze(0), r)
+
+
+# ----------------------------------------------------------------------------- many sequences
+# More than 1024 sequences (three rounds of the warp-wide cu_seqlens search),
+# most of them empty or a few tokens long.  dO is halved: with hundreds of
+# short sequences, a key near a sequence start collects a query's dO at a
+# weight near 1, so |dV| reaches ~5 with unit-variance dO; there bf16 output
+# rounding alone (half an ulp is 0.0156 in [4, 8)) plus the bf16 P operand
+# use up the 2e-2 absolute bound (an fp64 emulation of exactly those two
+# roundings gives 0.021 on the contiguous case).  Halved, |dV| stays below
+# ~3.3 and the emulated rounding below 0.011.
+@pytest.mark.parametrize("layout,lens,n", [
+    ("contiguous", [0, 2, 0, 0, 1, 3] * 200, 4),
+    ("zigzag", [0, 4, 0, 8] * 300, 2),
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_many_sequences(ra, layout, lens, n, causal):
+    h, d = 2, 128
+    cu = cu_seqlens(lens)
+    x = make_qkv(1, h, cu[-1], d, 4242 + len(lens), with_do=True)
+    x["do"] = (x["do"].float() * 0.5).to(torch.bfloat16)
+    scale = d ** -0.5
+    g = {k: ra.ring_attn_varlen_permute(v[0].transpose(0, 1).contiguous().cuda(), cu, layout, n, seq_dim=0)
+         for k, v in x.items()}
+    out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, causal, scale, layout=layout)
+    dq, dk, dv = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu, None, n, causal, scale,
+                                         layout=layout)
+    check_no_device_error(ra)
+    ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, causal, cu_seqlens=cu)
+    ref_g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, cu_seqlens=cu)
+
+    def back(t, seq_dim=0):
+        return ra.ring_attn_varlen_unpermute(t.contiguous(), cu, layout, n, seq_dim=seq_dim).cpu()
 
     assert_close("out", back(out).transpose(0, 1).unsqueeze(0), ref_o)
     assert_lse_close("lse", back(lse, 1).unsqueeze(0), ref_l)
