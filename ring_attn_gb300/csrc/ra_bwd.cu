@@ -515,10 +515,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y / p.H, h = blockIdx.y % p.H;
-  // causal: the later query tiles carry more work, start them first
-  const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  const int r = p.r_only >= 0 ? p.r_only : x / p.n_qtiles;
-  const int i0 = (x % p.n_qtiles) * kTileM;
+  // causal: the later query tiles carry more work, start them first (the
+  // batched zigzag split by chunk, so that every head's heaviest tiles lead)
+  int r, i0;
+  if (!VL && p.causal && p.layout == LAYOUT_ZIGZAG && p.r_only < 0 && p.L % (2 * kTileM) == 0) {
+    int qt;
+    zigzag_heavy_first((int)blockIdx.x, p.N, p.n_qtiles / 2, r, qt);
+    i0 = qt * kTileM;
+  } else {
+    const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    r = p.r_only >= 0 ? p.r_only : x / p.n_qtiles;
+    i0 = (x % p.n_qtiles) * kTileM;
+  }
   QRange qr;
   make_qrange(p, r, i0, kTileM, qr);
   const int nkt = (p.L + kTileN - 1) / kTileN;

@@ -107,11 +107,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int b = blockIdx.y / p.H;
   const int h = blockIdx.y % p.H;
-  // causal: the later query rows carry more work, start them first
-  const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  // causal: the later query rows carry more work, start them first (the
+  // batched zigzag split by chunk, so that every head's heaviest tiles lead)
   const int n_pairs = (p.L + kRowsPerCta - 1) / kRowsPerCta;
-  const int r = p.r_only >= 0 ? p.r_only : x / n_pairs;
-  const int i0 = (x % n_pairs) * kRowsPerCta;
+  int r, i0;
+  if (!VL && p.causal && p.layout == LAYOUT_ZIGZAG && p.r_only < 0 && p.L % (2 * kRowsPerCta) == 0) {
+    int pr;
+    zigzag_heavy_first((int)blockIdx.x, p.N, n_pairs / 2, r, pr);
+    i0 = pr * kRowsPerCta;
+  } else {
+    const int x = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    r = p.r_only >= 0 ? p.r_only : x / n_pairs;
+    i0 = (x % n_pairs) * kRowsPerCta;
+  }
   QRange cta;  // both query tiles together: decides which key tiles are visited
   make_qrange(p, r, i0, kRowsPerCta, cta);
   const int nkt = (p.L + kTileN - 1) / kTileN;

@@ -36,6 +36,19 @@ __device__ __forceinline__ int tok(const P& p, int r, int i) {
   return token_of(p.layout, p.N, p.L, r, i);
 }
 
+// Heavy-first order of query tiles for the batched causal zigzag layout.
+// Chunk c of the 2N (tokens [c C, (c+1) C)) sits in shard c (c < N) or
+// 2N-1-c, and a query tile of a later chunk sees more keys.  Rank k of a grid
+// of 2N * tpc tiles (tpc per chunk) is mapped to (shard, local tile) so that
+// every head's heaviest tiles start first and the lightest end the grid (the
+// plain reversed order left the heaviest chunk, in shard 0, to the end).
+__device__ __forceinline__ void zigzag_heavy_first(int k, int N, int tpc, int& shard, int& tile) {
+  const int ch = 2 * N - 1 - k / tpc;
+  const int t = tpc - 1 - k % tpc;
+  shard = ch < N ? ch : 2 * N - 1 - ch;
+  tile = (ch < N ? 0 : tpc) + t;
+}
+
 // Query rows [i0, i0 + rows) of Q shard r; the valid ones end at i_last.
 struct QRange {
   int r, i0, i_last;
