@@ -215,12 +215,17 @@ def _shrink(s, h):
 
 
 # ----------------------------------------------------------------------------- our arm
-def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3):
+def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
     """fwd + bwd of a packed varlen workload, inputs resident in layout order,
-    timed with CUDA events around `steps` steps on the current stream."""
+    timed with CUDA events around `steps` steps on the current stream (heads:
+    fewer heads, for profiling captures)."""
+    import dataclasses
+
     from workload import WORKLOADS, cu_seqlens, make_workload_inputs
 
     w = WORKLOADS[wid]
+    if heads:
+        w = dataclasses.replace(w, h=int(heads))
     cu = torch.tensor(cu_seqlens(w.seq_lengths()), dtype=torch.int32)
     x = make_workload_inputs(w, device=str(dev))
     g = {n: ra.ring_attn_varlen_permute(t[0].contiguous(), cu, w.layout, w.n_shards, seq_dim=1) for n, t in x.items()}
@@ -273,6 +278,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--seq", type=int, default=None, help="smaller sequence length (profiling cases only)")
     ap.add_argument("--heads", type=int, default=None, help="fewer heads (profiling cases only)")
+    ap.add_argument("--varlen", type=int, choices=[5, 6], default=None,
+                    help="run only the varlen leg of this workload and print its figures (profiling aid)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -304,6 +311,12 @@ def main():
     ra.load()
     dev = torch.device("cuda", local)
     peaks = _peaks()
+    if args.varlen:
+        # profiling aid, not a bench line: one varlen workload (optionally fewer heads) alone
+        res = _varlen_leg(ra, torch, args.varlen, peaks, dev, steps=args.steps, warmup=args.warmup, heads=args.heads)
+        if rank == 0:
+            _emit({"varlen_only": args.varlen, **res})
+        return 0
     scale = D ** -0.5
 
     # inputs: seeded on the device, original order, then moved to layout order by the library
