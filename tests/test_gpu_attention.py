@@ -277,6 +277,34 @@ def test_varlen_many_sequences(ra, layout, lens, n, causal):
         assert_close(name, back(got).transpose(0, 1).unsqueeze(0), r)
 
 
+@pytest.mark.parametrize("n_seqs", [1, 31, 32, 33, 1023, 1024, 1025])
+def test_varlen_search_boundaries(ra, n_seqs):
+    """cu_seqlens sizes at the warp-wide search's round boundaries (32, 1024
+    entries), random lengths of 0-12 tokens (empty sequences first and last
+    included), causal contiguous shards; dO halved as in the many-sequence case."""
+    rng = np.random.default_rng(77 + n_seqs)
+    lens = [int(x) for x in rng.integers(0, 13, n_seqs)]
+    lens[0] = 0
+    lens[-1] = 0 if n_seqs > 1 else 16
+    lens[n_seqs // 2] += 4 - sum(lens) % 4  # total divisible by the 4 shards
+    h, d, n = 1, 64, 4
+    cu = cu_seqlens(lens)
+    x = make_qkv(1, h, cu[-1], d, 900 + n_seqs, with_do=True)
+    x["do"] = (x["do"].float() * 0.5).to(torch.bfloat16)
+    scale = d ** -0.5
+    g = {k: v[0].transpose(0, 1).contiguous().cuda() for k, v in x.items()}
+    out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, True, scale)
+    dq, dk, dv = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu, None, n, True, scale)
+    check_no_device_error(ra)
+    ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, True, cu_seqlens=cu)
+    ref_g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], scale, True, cu_seqlens=cu)
+    back = lambda t: t.cpu().transpose(0, 1).unsqueeze(0)  # noqa: E731
+    assert_close("out", back(out), ref_o)
+    assert_lse_close("lse", lse.cpu().unsqueeze(0), ref_l)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref_g):
+        assert_close(name, back(got), r)
+
+
 # ----------------------------------------------------------------------------- llama3 form
 @pytest.mark.parametrize("lens,n", [
     ([100, 1, 300, 27, 84], 4),
