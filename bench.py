@@ -234,12 +234,12 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
     lse = torch.empty((w.h, w.s), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
     ws = torch.empty(ra.ring_attn_workspace_size(1, 1, w.h, w.s, w.d, w.n_shards), dtype=torch.uint8, device=dev)
-    cu_host = cu.contiguous()
+    cuw = ra.CuSeqlens(cu, dev)  # host and device copies made once: the timed steps copy nothing
 
     def step():
-        ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu_host, None, w.n_shards, w.causal, w.scale, out=out, lse=lse,
+        ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cuw, None, w.n_shards, w.causal, w.scale, out=out, lse=lse,
                                 layout=w.layout)
-        ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu_host, None, w.n_shards, w.causal,
+        ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cuw, None, w.n_shards, w.causal,
                                 w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, layout=w.layout)
 
     for _ in range(warmup):
@@ -264,8 +264,72 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
     tf = 2.5 * w.fwd_flops() / (ms * 1e-3) / 1e12
     return {"workload": f"{w.name}: h{w.h} total {w.s} d{w.d}, {w.varlen_seqs} seqs, {w.n_shards} {w.layout} shards",
             "ms_per_step": ms, "tflops": tf, "frac_of_peak": tf / peaks["bf16_sustained"],
+            "frac_of_burst": tf / peaks["bf16"],
             "kernel_ms": {n: t / max(c, 1) for n, (t, c) in kt.items()},
             "flop_convention": "fwd = sum_k 4*h*L_k^2*d/2; fwd+bwd = 2.5 x fwd"}
+
+
+def _batched_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3):
+    """One of the pages' batched workloads other than the headline one (the
+    contiguous 16k forward, the stripe 128k forward+backward): inputs resident
+    in layout order, `steps` steps timed with CUDA events on the current
+    stream, then a separate pass split per kernel."""
+    from workload import WORKLOADS, make_workload_inputs
+
+    w = WORKLOADS[wid]
+    x = make_workload_inputs(w, device=str(dev))
+    g = {n: ra.ring_attn_permute(t, w.layout, w.n_shards) for n, t in x.items()}
+    del x
+    out = torch.empty_like(g["q"])
+    lse = torch.empty((w.b, w.h, w.s), dtype=torch.float32, device=dev)
+    if w.backward:
+        dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+        ws = torch.empty(ra.ring_attn_workspace_size(1, w.b, w.h, w.s, w.d, w.n_shards), dtype=torch.uint8,
+                         device=dev)
+
+    def step():
+        ra.ring_attn_fwd(g["q"], g["k"], g["v"], w.layout, w.n_shards, w.causal, w.scale, out=out, lse=lse)
+        if w.backward:
+            ra.ring_attn_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, w.layout, w.n_shards, w.causal, w.scale,
+                             dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ra.ring_attn_timing_enable(True)
+    for _ in range(2):
+        step()
+    names = ("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq") if w.backward else ("fwd",)
+    kt = {n: ra.ring_attn_timing_read(n) for n in names}
+    ra.ring_attn_timing_enable(False)
+    st, info = ra.ring_attn_check_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} info {info:#x} in the {w.name} leg")
+    kms = {n: t / max(c, 1) for n, (t, c) in kt.items()}
+    fwd_f = w.fwd_flops()
+    fwd_tf = fwd_f / (kms["fwd"] * 1e-3) / 1e12
+    res = {"workload": f"{w.name}: b{w.b} h{w.h} s{w.s} d{w.d}, {w.n_shards} {w.layout} shards, "
+                       f"{'causal' if w.causal else 'non-causal'}",
+           "fwd_tflops": fwd_tf, "fwd_frac_of_burst": fwd_tf / peaks["bf16"],
+           "fwd_frac_of_sustained": fwd_tf / peaks["bf16_sustained"], "kernel_ms": kms, "ms_per_step": ms}
+    if w.backward:
+        tf = 2.5 * fwd_f / (ms * 1e-3) / 1e12
+        res.update({"fwd_bwd_tflops": tf, "fwd_bwd_frac_of_burst": tf / peaks["bf16"],
+                    "fwd_bwd_frac_of_sustained": tf / peaks["bf16_sustained"],
+                    "fwd_bwd_tflops_3p5x": 3.5 * fwd_f / (ms * 1e-3) / 1e12,
+                    "dkdv_tflops_performed": 2.0 * fwd_f / (kms["bwd_dkdv"] * 1e-3) / 1e12,
+                    "dq_tflops_performed": 1.5 * fwd_f / (kms["bwd_dq"] * 1e-3) / 1e12})
+    else:
+        res["fwd_tflops_step"] = fwd_f / (ms * 1e-3) / 1e12
+    res["flop_convention"] = "fwd = 4*b*h*s^2*d (/2 causal); fwd+bwd = 2.5 x fwd"
+    return res
 
 
 def main():
@@ -276,6 +340,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="skip the contiguous-16k and stripe-128k legs")
     ap.add_argument("--seq", type=int, default=None, help="smaller sequence length (profiling cases only)")
     ap.add_argument("--heads", type=int, default=None, help="fewer heads (profiling cases only)")
     ap.add_argument("--varlen", type=int, choices=[5, 6], default=None,
@@ -391,6 +456,7 @@ def main():
     d_tflops = d_flop / (d_ms * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": d_tflops, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": d_tflops / peak_sus, "traffic": _profiled_traffic(d_prof, d_src + common),
+                "frac_of_burst": d_tflops / peaks["bf16"],
                 "algorithmic_flop_per_launch": d_flop, "peak_kind": f"bf16 sustained ({peaks['source']})",
                 "launch_ms": d_ms}
     result = {
@@ -402,6 +468,7 @@ def main():
                    "l2": "no flush: inputs larger than L2 (q, k, v, dO 512 MiB each)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd": {"tflops": fwd_tflops, "ms": fwd_ms, "frac_of_peak": fwd_tflops / peak_sus,
+                "frac_of_burst": fwd_tflops / peaks["bf16"],
                 "traffic": _profiled_traffic("ring_fwd_kernel_zigzag_h32_s64k.md",
                                              ["ring_attn_gb300/csrc/ra_fwd.cu"] + common)},
         "bwd": {"tflops": bwd_tflops, "ms": bwd_ms, "frac_of_peak": bwd_tflops / peak_sus,
@@ -409,6 +476,7 @@ def main():
                 "dkdv_ms": dkdv_ms, "dkdv_tflops_performed": 2.0 * FWD_FLOP / (dkdv_ms * 1e-3) / 1e12,
                 "dq_ms": dq_ms, "dq_tflops_performed": 1.5 * FWD_FLOP / (dq_ms * 1e-3) / 1e12, "pre_ms": pre_ms},
         "fwd_bwd_frac_of_peak": value / world / peak_sus,
+        "fwd_bwd_frac_of_burst": value / world / peaks["bf16"],
         "fwd_bwd_tflops_3p5x": job_tflops(world, STEP_FLOP_ALG, ms),
         "roofline": roofline, "gpu_launches": launches, "clocks": clk,
         "peaks": peaks,
@@ -521,6 +589,14 @@ def main():
                                   "kind": "oracle", "seconds": dt,
                                   "sample": f"fp64 numpy oracle fwd+bwd of the causal prefix of {n} tokens of "
                                             f"head 0 (exact sub-problem), same 2.5x flop convention"}
+    # ---- the pages' other batched workloads: contiguous 16k forward, stripe 128k fwd+bwd
+    if not (args.seq or args.heads or args.no_legs):
+        del x, g, q, k, v, do, out, lse, dq, dk, dv, ws
+        if not args.no_e2e:
+            del hin, hout, hlse, dbuf, rbuf, lbuf
+        torch.cuda.empty_cache()
+        result["config2"] = _batched_leg(ra, torch, 2, peaks, dev)
+        result["config4"] = _batched_leg(ra, torch, 4, peaks, dev)
     if rank == 0:
         _emit(result)
     if dist is not None:

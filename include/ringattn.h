@@ -154,7 +154,12 @@ ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tens
  *   Set-up: the first call on each device looks up the array's device address
  *   with that device current (cudaGetSymbolAddress, which loads the library's
  *   device code if it is not loaded yet); make that first call before any
- *   stream capture begins.  Later calls on the device reuse the address.
+ *   stream capture begins.  Later calls on the device reuse the address, so
+ *   do not call it again on a device after cudaDeviceReset in the same
+ *   process: the cached address would be stale.
+ *   Errors: every argument error of ring_attn_bwd is reported first, with the
+ *   same status; only a valid problem that is too large gets
+ *   RA_ERR_SCRATCH_LIMIT.
  *   The array keeps the last call's contents; nothing in it needs to start at
  *   zero, because every call writes all of it that it reads before reading it.
  *   Races: every call on a device shares the array.  Calls ordered on one
@@ -225,7 +230,10 @@ ra_status ring_attn_llama3_varlen_bwd(const ra_tensor* dout, const ra_tensor* q,
  *   y[..., p, ...] = x[..., g(p), ...], g(p) = original token at layout position p.
  * ring_attn_unpermute: the inverse, x[..., g(p), ...] = y[..., p, ...].
  *   x, y: same shape, 1-D to 4-D, bf16 or fp32 (same dtype); the dimensions
- *   after seq_dim must be packed (row-major contiguous).  A bit copy. */
+ *   after seq_dim must be packed (row-major contiguous).  A bit copy.
+ *   x and y must not overlap in memory (no in-place permutation: rows are
+ *   gathered by many blocks at once); overlapping byte ranges get
+ *   RA_ERR_INVALID_ARG before any launch. */
 ra_status ring_attn_permute(const ra_tensor* x, ra_tensor* y, int32_t layout, int32_t n_shards, int32_t seq_dim,
                             void* stream);
 ra_status ring_attn_unpermute(const ra_tensor* y, ra_tensor* x, int32_t layout, int32_t n_shards, int32_t seq_dim,

@@ -22,7 +22,7 @@ __all__ = [
     "KERNELS", "RA_STATIC_SCRATCH_BYTES", "ring_attn_qkvpacked_fwd", "ring_attn_qkvpacked_bwd", "ring_attn_kvpacked_fwd",
     "ring_attn_kvpacked_bwd", "ring_attn_varlen_qkvpacked_fwd", "ring_attn_varlen_qkvpacked_bwd",
     "ring_attn_varlen_kvpacked_fwd", "ring_attn_varlen_kvpacked_bwd", "ring_attn_varlen_permute",
-    "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd",
+    "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd", "CuSeqlens",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
@@ -235,13 +235,42 @@ def ring_attn_bwd_static_scratch(dout, q, k, v, out, lse, layout="contiguous", n
     return dq, dk, dv
 
 
+class CuSeqlens:
+    """One cu_seqlens prepared once for repeated varlen calls.
+
+    Holds the int32 host copy that the library validates before each launch and
+    the device copy that its kernels read, so that a call given a CuSeqlens
+    copies and allocates nothing for it (a plain list or tensor passed to a
+    varlen call is copied to the device on every call)."""
+
+    def __init__(self, cu_seqlens, device):
+        if isinstance(cu_seqlens, torch.Tensor):
+            host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+        else:
+            host = torch.tensor(list(cu_seqlens), dtype=torch.int32)
+        if host.dim() != 1 or host.numel() < 2:
+            raise ValueError("cu_seqlens must be a 1-D array of n_seqs + 1 prefix sums")
+        self.host = host
+        self.dev = host.to(device)
+        self.n_seqs = host.numel() - 1
+        self.total = int(host[-1])
+        self.max_seqlen = int((host[1:] - host[:-1]).max())
+
+
+def _max_len(cu_seqlens, host):
+    if isinstance(cu_seqlens, CuSeqlens):
+        return cu_seqlens.max_seqlen
+    return int((host[1:] - host[:-1]).max())
+
+
 def _cu_pair(cu_seqlens, device):
-    if isinstance(cu_seqlens, torch.Tensor):
-        host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
-    else:
-        host = torch.tensor(list(cu_seqlens), dtype=torch.int32)
-    dev = host.to(device)
-    return host, dev
+    """(host, device) copies of cu_seqlens; a CuSeqlens is used as it is."""
+    if isinstance(cu_seqlens, CuSeqlens):
+        if cu_seqlens.dev.device != torch.device(device):
+            raise ValueError(f"CuSeqlens was prepared for {cu_seqlens.dev.device}, not {device}")
+        return cu_seqlens.host, cu_seqlens.dev
+    c = CuSeqlens(cu_seqlens, device)
+    return c.host, c.dev
 
 
 def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
@@ -255,7 +284,7 @@ def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causa
     n = host.numel() - 1
     total = int(host[-1])
     if max_seqlen is None:
-        max_seqlen = int((host[1:] - host[:-1]).max())
+        max_seqlen = _max_len(cu_seqlens, host)
     h = q.shape[1] if q.shape[0] == total else q.shape[0]
     d = q.shape[2]
     out = torch.empty_like(q) if out is None else out
@@ -278,7 +307,7 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
     n = host.numel() - 1
     total = int(host[-1])
     if max_seqlen is None:
-        max_seqlen = int((host[1:] - host[:-1]).max())
+        max_seqlen = _max_len(cu_seqlens, host)
     h = q.shape[1] if q.shape[0] == total else q.shape[0]
     d = q.shape[2]
     dq = torch.empty_like(q) if dq is None else dq
@@ -312,7 +341,7 @@ def ring_attn_llama3_varlen_fwd(q, k, v, cu_seqlens, rank, n_shards, causal=True
     n = host.numel() - 1
     total = int(host[-1])
     if max_seqlen is None:
-        max_seqlen = int((host[1:] - host[:-1]).max())
+        max_seqlen = _max_len(cu_seqlens, host)
     L = total // int(n_shards)
     h, d = _heads_of(q, L), q.shape[2]
     out = torch.empty_like(q) if out is None else out
@@ -334,7 +363,7 @@ def ring_attn_llama3_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, rank, n_sha
     n = host.numel() - 1
     total = int(host[-1])
     if max_seqlen is None:
-        max_seqlen = int((host[1:] - host[:-1]).max())
+        max_seqlen = _max_len(cu_seqlens, host)
     L = total // int(n_shards)
     h, d = _heads_of(q, L), q.shape[2]
     dq = torch.empty_like(q) if dq is None else dq

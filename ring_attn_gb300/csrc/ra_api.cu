@@ -197,6 +197,25 @@ struct TimedLaunch {
   } while (0)
 
 // Shared forward: fused ring (step < 0) or one ring step.
+// The argument checks of every backward entry point, made before anything
+// touches the device or the workspace.
+ra_status bwd_check_args(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
+                         int32_t layout, int32_t n_shards, int32_t causal, float scale, const Bhsd& dq,
+                         const Bhsd& dk, const Bhsd& dv, int32_t rank) {
+  if (!same_shape(k, v) || !same_shape(k, dk) || !same_shape(k, dv) || !same_shape(q, out) ||
+      !same_shape(q, dout) || !same_shape(q, dq))
+    return RA_ERR_INVALID_ARG;
+  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
+  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
+    return RA_ERR_INVALID_ARG;
+  if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
+  RA_TRY(check_layout(layout, n_shards, k.s));
+  RA_TRY(check_scale(scale));
+  if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
+  if (k.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  return RA_OK;
+}
+
 // rank >= 0: one rank of the llama3 form: q and o hold that rank's L = S / N
 // rows (the contiguous slice [rank*L, (rank+1)*L)), k and v all S rows.
 ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout, int32_t n_shards, int32_t causal,
@@ -265,17 +284,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
                      const float* lse, long long lsb, long long lsh, long long lss, int32_t layout, int32_t n_shards,
                      int32_t causal, float scale, const Bhsd& dq, const Bhsd& dk, const Bhsd& dv, void* ws,
                      size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1) {
-  if (!same_shape(k, v) || !same_shape(k, dk) || !same_shape(k, dv) || !same_shape(q, out) ||
-      !same_shape(q, dout) || !same_shape(q, dq))
-    return RA_ERR_INVALID_ARG;
-  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
-  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
-    return RA_ERR_INVALID_ARG;
-  if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
-  RA_TRY(check_layout(layout, n_shards, k.s));
-  RA_TRY(check_scale(scale));
-  if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
-  if (k.s > (1LL << 30) || q.b * q.h > 65535) return RA_ERR_UNSUPPORTED;
+  RA_TRY(bwd_check_args(dout, q, k, v, out, layout, n_shards, causal, scale, dq, dk, dv, rank));
   const int stat_N = rank >= 0 ? 1 : n_shards;  // shards whose rows the statistics hold
   if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, stat_N)) return RA_ERR_WORKSPACE;
   const int stat_L = (int)stat_rows_per_shard(q.s, stat_N);
@@ -563,7 +572,9 @@ ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q
   RA_TRY(check_bhsd(dv, &vdv));
   long long lsb, lsh, lss;
   RA_TRY(check_lse(lse, vq.b, vq.h, vq.s, &lsb, &lsh, &lss));
-  RA_TRY(check_layout(layout, n_shards, vq.s));
+  // Every argument check of ring_attn_bwd comes first, so a bad argument gets
+  // the same status from both calls; only then the size of the array.
+  RA_TRY(bwd_check_args(vdo, vq, vk, vv, vo, layout, n_shards, causal, softmax_scale, vdq, vdk, vdv, -1));
   if (bwd_ws_bytes(vq.b, vq.h, vq.s, n_shards) > RA_STATIC_SCRATCH_BYTES) return RA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   RA_TRY(static_scratch(&scratch));
@@ -666,6 +677,26 @@ ra_status ring_attn_llama3_varlen_bwd(const ra_tensor* dout, const ra_tensor* q,
                     stream, rank);
 }
 
+// Byte span [first, last] that a tensor's strides can reach (negative strides
+// are refused by the callers' packing checks, but are handled here anyway).
+static void byte_span(const ra_tensor* t, int es, uintptr_t* lo, uintptr_t* hi) {
+  long long mn = 0, mx = 0;
+  for (int i = 0; i < t->ndim; ++i) {
+    const long long reach = (t->shape[i] - 1) * t->stride[i];
+    if (reach < 0) mn += reach; else mx += reach;
+  }
+  const uintptr_t base = reinterpret_cast<uintptr_t>(t->data);
+  *lo = base + (uintptr_t)(mn * es);
+  *hi = base + (uintptr_t)(mx * es) + (uintptr_t)(es - 1);
+}
+
+static bool ranges_overlap(const ra_tensor* a, const ra_tensor* b, int es) {
+  uintptr_t alo, ahi, blo, bhi;
+  byte_span(a, es, &alo, &ahi);
+  byte_span(b, es, &blo, &bhi);
+  return alo <= bhi && blo <= ahi;
+}
+
 static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t layout, int32_t n_shards,
                                 int32_t seq_dim, int inverse, const int32_t* cu_dev, int32_t n_seqs, void* stream) {
   if (!src || !dst || !src->data || !dst->data) return RA_ERR_INVALID_ARG;
@@ -686,6 +717,9 @@ static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t la
   }
   const int es = src->dtype == RA_FP32 ? 4 : 2;
   if (!aligned(src->data, es) || !aligned(dst->data, es)) return RA_ERR_ALIGNMENT;
+  // Rows are gathered by many blocks at once, so a destination that overlaps
+  // the source would be read after other blocks overwrote it: refuse it.
+  if (ranges_overlap(src, dst, es)) return RA_ERR_INVALID_ARG;
   PermuteArgs a;
   memset(&a, 0, sizeof(a));
   a.src = src->data;

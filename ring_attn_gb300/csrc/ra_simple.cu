@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
     for (int t0 = (int)blockIdx.x * rows_per_block; t0 + wrow < stat_L; t0 += kPreUnroll * istride) {
       const int i0 = t0 + rloc;
       uint4 x[kPreUnroll], y[kPreUnroll];
+      float l[kPreUnroll];
+      // every load of the turn first, the row's lse included: loaded after the
+      // reduction it would add one memory latency per row to each turn
 #pragma unroll
       for (int u = 0; u < kPreUnroll; ++u) {
         const int i = i0 + u * istride;
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
         const long long p = (long long)r * L + i;  // layout position
         x[u] = real ? __ldcs(reinterpret_cast<const uint4*>(dsrc + p * dout.ss) + part) : make_uint4(0, 0, 0, 0);
         y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + p * out.ss) + part) : make_uint4(0, 0, 0, 0);
+        l[u] = real && part == 0 ? __ldcs(lsrc + p * lse.ss) : INFINITY;
       }
 #pragma unroll
       for (int u = 0; u < kPreUnroll; ++u) {
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out
         if (part == 0 && i < stat_L) {
           const long long row = bhr * stat_L + i;
           nD[row] = -acc;
-          nlse2[row] = i < L ? lsrc[((long long)r * L + i) * lse.ss] * -1.4426950408889634f : -INFINITY;
+          nlse2[row] = l[u] * -1.4426950408889634f;  // padding rows: +inf * -log2(e) = -inf
         }
       }
     }

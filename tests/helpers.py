@@ -36,7 +36,8 @@ def assert_lse_close(name, got, ref, tol=TOL_LSE):
     assert got.shape == ref.shape
     both_inf = np.isneginf(got) & np.isneginf(ref)
     assert np.array_equal(np.isneginf(got), np.isneginf(ref)), f"{name}: -inf pattern differs"
-    err = np.abs(np.where(both_inf, 0.0, got - ref))
+    err = np.zeros_like(got)
+    err[~both_inf] = np.abs(got[~both_inf] - ref[~both_inf])
     mx = float(err.max()) if err.size else 0.0
     assert mx <= tol, f"{name}: max-abs {mx:.3e} > {tol}"
 

@@ -184,12 +184,36 @@ def test_lse_merge_rejects_bad_shapes(lib):
 
 def test_permute_rejects_bad_arguments(lib):
     x = _fake((1, 2, 12, 8))
-    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 10, 8))), 0, 2, 2, None) == 1
-    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8))), 1, 4, 2, None) == 1  # 12 % 8
-    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8))), 0, 2, 4, None) == 1
+    far = 0x100000  # a destination that does not overlap x, so each refusal below has its own cause
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 10, 8), data=far)), 0, 2, 2, None) == 1
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8), data=far)), 1, 4, 2,
+                                 None) == 1  # 12 % 8
+    assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(_fake((1, 2, 12, 8), data=far)), 0, 2, 4, None) == 1
     # dims after seq_dim must be packed
     y = _fake((1, 2, 12, 8), strides=(384, 192, 16, 2))
-    assert lib.ring_attn_permute(ctypes.byref(y), ctypes.byref(_fake((1, 2, 12, 8))), 0, 2, 2, None) == 1
+    assert lib.ring_attn_permute(ctypes.byref(y), ctypes.byref(_fake((1, 2, 12, 8), data=far)), 0, 2, 2, None) == 1
+
+
+def test_permute_refuses_overlapping_buffers(lib):
+    """In place, or partly overlapping: refused before any launch (rows would be
+    read after other blocks overwrote them)."""
+    x = _fake((1, 2, 12, 8))  # 384 bytes at 0x10000
+    for lay in (0, 1, 2):
+        assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(x), lay, 2, 2, None) == 1
+        assert lib.ring_attn_unpermute(ctypes.byref(x), ctypes.byref(x), lay, 2, 2, None) == 1
+    for off in (2, 128, 382):
+        y = _fake((1, 2, 12, 8), data=0x10000 + off)
+        assert lib.ring_attn_permute(ctypes.byref(x), ctypes.byref(y), 1, 2, 2, None) == 1
+        y = _fake((1, 2, 12, 8), data=0x10000 - off)
+        assert lib.ring_attn_unpermute(ctypes.byref(x), ctypes.byref(y), 1, 2, 2, None) == 1
+    # a strided source whose rows interleave with the destination's
+    xs = _fake((1, 2, 12, 8), strides=(384, 192, 16, 1))
+    y = _fake((1, 2, 12, 8), data=0x10000 + 16)
+    assert lib.ring_attn_permute(ctypes.byref(xs), ctypes.byref(y), 0, 2, 2, None) == 1
+    x32 = _fake((12, 4), ra.RA_FP32)
+    assert lib.ring_attn_varlen_permute(ctypes.byref(x32), ctypes.byref(x32), ctypes.c_void_p(0x1000),
+                                        ctypes.cast((ctypes.c_int32 * 3)(0, 8, 12), ctypes.c_void_p), 2, 0, 2, 0,
+                                        None) == 1
 
 
 def test_knobs(lib):

@@ -241,13 +241,13 @@ def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d):
 
 # ----------------------------------------------------------------------------- many sequences
 # More than 1024 sequences (three rounds of the warp-wide cu_seqlens search),
-# most of them empty or a few tokens long.  dO is halved: with hundreds of
-# short sequences, a key near a sequence start collects a query's dO at a
-# weight near 1, so |dV| reaches ~5 with unit-variance dO; there bf16 output
-# rounding alone (half an ulp is 0.0156 in [4, 8)) plus the bf16 P operand
-# use up the 2e-2 absolute bound (an fp64 emulation of exactly those two
-# roundings gives 0.021 on the contiguous case).  Halved, |dV| stays below
-# ~3.3 and the emulated rounding below 0.011.
+# most of them empty or a few tokens long.  dO is halved, a reading of the
+# tolerance: with hundreds of short sequences a key near a sequence start collects
+# its queries' dO at weights near 1, so |dV| reaches ~5 with unit-variance dO,
+# and there the bf16 output rounding plus the bf16 P operand alone use up the
+# 2e-2 absolute bound.  tests/test_tolerance_readings.py emulates exactly those
+# two roundings on the fp64 oracle: 0.0207 (causal) and 0.0192 with unit dO,
+# 0.0104 and 0.0096 with dO halved.
 @pytest.mark.parametrize("layout,lens,n", [
     ("contiguous", [0, 2, 0, 0, 1, 3] * 200, 4),
     ("zigzag", [0, 4, 0, 8] * 300, 2),
@@ -281,7 +281,8 @@ def test_varlen_many_sequences(ra, layout, lens, n, causal):
 def test_varlen_search_boundaries(ra, n_seqs):
     """cu_seqlens sizes at the warp-wide search's round boundaries (32, 1024
     entries), random lengths of 0-12 tokens (empty sequences first and last
-    included), causal contiguous shards; dO halved as in the many-sequence case."""
+    included), causal contiguous shards; dO halved as in the many-sequence case
+    (the tolerance reading that tests/test_tolerance_readings.py supports)."""
     rng = np.random.default_rng(77 + n_seqs)
     lens = [int(x) for x in rng.integers(0, 13, n_seqs)]
     lens[0] = 0

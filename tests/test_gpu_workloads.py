@@ -109,6 +109,27 @@ def _check_keys(w, res, h, keys):
     assert_close(f"dv h{h}", res["dv"][0, h, keys].cpu(), dv)
 
 
+def _head_stats(w, res, h):
+    """out, lse and D = rowsum(dO * out) of EVERY row of head h, from the fp64
+    oracle's forward (row blocks of 1024 queries, so host memory stays bounded)."""
+    cu = res.get("cu")
+    q, k, v, do = (res["x"][n][0:1, h:h + 1].cpu() for n in ("q", "k", "v", "do"))
+    out, lse = oracle.attention_fwd(q, k, v, w.scale, w.causal, cu_seqlens=cu, row_block=1024)
+    D = (f64(do)[0, 0] * out[0, 0]).sum(axis=-1)
+    return out[0, 0], lse[0, 0], D
+
+
+def _check_keys_all_rows(w, res, h, keys, stats):
+    """dk, dv of selected keys against the oracle, with lse and D of all rows."""
+    cu = res.get("cu")
+    q, k, v, do = (res["x"][n][0, h].cpu() for n in ("q", "k", "v", "do"))
+    keys = np.asarray(sorted(keys))
+    _, lse, D = stats
+    dk, dv = oracle.key_grads(q, k, v, do, keys, lse, D, w.scale, w.causal, cu)
+    assert_close(f"dk h{h} ({len(keys)} keys from {keys.min()})", res["dk"][0, h, keys].cpu(), dk)
+    assert_close(f"dv h{h} ({len(keys)} keys from {keys.min()})", res["dv"][0, h, keys].cpu(), dv)
+
+
 def _check_sums(w, res):
     dk = res["dk"][0].float()
     dv = res["dv"][0].float()
@@ -142,12 +163,25 @@ def test_causal_contiguous_fwd_h32_s16k(ra):
 
 @pytest.mark.parametrize("wid", [3, 4])
 def test_causal_fwd_bwd_full_size(ra, wid):
+    """Sampled rows of two heads; then, for head 0, out and lse of every row and
+    dk, dv of the keys that every shard's queries see: the first 128-token tile
+    (zigzag: the start of chunk 0 of shard 0; stripe: local tile 0 of every
+    shard), keys around the middle of the sequence and at chunk boundaries,
+    and late keys, all against the oracle with lse and D of all rows."""
     w = WORKLOADS[wid]
     res = _run(ra, w)
     _check_rows(w, res, heads=[0, w.h - 1], n_rows=32, seed=wid)
+    stats = _head_stats(w, res, 0)
+    assert_close("out h0 (all rows)", res["out"][0, 0].cpu(), stats[0])
+    assert_lse_close("lse h0 (all rows)", res["lse"][0, 0].cpu(), stats[1])
     rng = np.random.default_rng(wid)
-    keys = set((w.s - 1 - rng.integers(0, 2048, size=12)).tolist()) | {w.s - 1, w.s - 2048}
-    _check_keys(w, res, 0, keys)
+    c = w.s // (2 * w.n_shards)
+    _check_keys_all_rows(w, res, 0, range(0, 128), stats)
+    mid = set(range(w.s // 2 - 8, w.s // 2 + 8)) | {c - 1, c, 3 * c - 1, 3 * c, 7 * c + 5}
+    mid |= set(rng.integers(0, w.s, size=16).tolist())
+    _check_keys_all_rows(w, res, 0, mid, stats)
+    late = set((w.s - 1 - rng.integers(0, 2048, size=12)).tolist()) | {w.s - 1, w.s - 2048}
+    _check_keys_all_rows(w, res, 0, late, stats)
     _check_sums(w, res)
     for n in ("out", "dq", "dk", "dv"):
         assert torch.isfinite(res[n].float()).all(), n
@@ -166,5 +200,12 @@ def test_varlen_fwd_bwd_full_size(ra, wid):
         keys.update(rng.integers(cu[sg], cu[sg + 1], size=4).tolist())
         keys.update({int(cu[sg]), int(cu[sg + 1] - 1)})
     _check_keys(w, res, 0, keys)
+    # every row of head 0, and the first 128 keys of the longest sequence (the
+    # keys with the most queries) with lse and D of all rows
+    stats = _head_stats(w, res, 0)
+    assert_close("out h0 (all rows)", res["out"][0, 0].cpu(), stats[0])
+    assert_lse_close("lse h0 (all rows)", res["lse"][0, 0].cpu(), stats[1])
+    longest = int(np.argmax(np.diff(cu)))
+    _check_keys_all_rows(w, res, 0, range(int(cu[longest]), int(cu[longest]) + 128), stats)
     for n in ("out", "dq", "dk", "dv"):
         assert torch.isfinite(res[n].float()).all(), n
