@@ -263,11 +263,15 @@ size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int
  * *info (optional) gets the failing wait site and block. */
 ra_status ring_attn_check_device_error(void* stream, int32_t* info);
 
-/* Debug knobs (process-wide).  RA_KNOB_WAIT_LIMIT_NS: the bounded-wait limit
- * in ns (default 4e9).  RA_KNOB_DEBUG_FLAGS: bit 0 makes the forward's TMA
- * producer skip the Q tile load, so that every consumer's bounded wait runs
- * out: a test of the timeout path that hangs nothing. */
-typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1 } ra_knob;
+/* Knobs (process-wide).  RA_KNOB_WAIT_LIMIT_NS: the bounded-wait limit in ns
+ * (default 4e9).  RA_KNOB_DEBUG_FLAGS: bit 0 makes the forward's TMA producer
+ * skip the Q tile load, so that every consumer's bounded wait runs out: a test
+ * of the timeout path that hangs nothing.  RA_KNOB_DKDV_PAIR: 1 (default) runs
+ * the backward's dK / dV pass at head_dim 128 on CTA pairs (two SMs share each
+ * M = 256 tensor-core MMA, halving each SM's operand reads from shared memory);
+ * 0 runs the one-CTA kernel, which head_dim 64 always uses.  Both give the
+ * same results up to fp32 summation order. */
+typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1, RA_KNOB_DKDV_PAIR = 2 } ra_knob;
 ra_status ring_attn_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing (process-wide, off by default; one device per process).

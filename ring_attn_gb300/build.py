@@ -12,8 +12,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
-SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_simple.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("ra_device.cuh", "ra_internal.h", "ra_tiles.cuh")] + [
+SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_dkdv_pair.cu", "ra_simple.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("ra_device.cuh", "ra_internal.h", "ra_tiles.cuh", "ra_bwd_common.cuh")] + [
     os.path.join(ROOT, "include", "ringattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

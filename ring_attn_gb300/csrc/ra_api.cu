@@ -20,6 +20,7 @@ __device__ int g_dev_err[2];  // [0] error code, [1] site | block << 8
 std::mutex g_mu;
 unsigned long long g_wait_limit_ns = 4000000000ull;
 int g_debug_flags = 0;
+int g_dkdv_pair = 1;  // head_dim 128: the dK / dV pass on CTA pairs
 int* g_err_ptr[64] = {nullptr};
 
 ra_status dev_ctl(DevCtl* c) {
@@ -63,8 +64,8 @@ struct Bhsd {
   long long sb, sh, ss;
 };
 
-// TMA map over (d, s, h, b) with 128 x 64 boxes and 128-byte swizzle.
-ra_status make_tmap(const Bhsd& t, CUtensorMap* m) {
+// TMA map over (d, s, h, b) with boxes of 64 head dims by box_rows rows and 128-byte swizzle.
+ra_status make_tmap(const Bhsd& t, CUtensorMap* m, int box_rows = kTileM) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return RA_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)t.d, (cuuint64_t)t.s, (cuuint64_t)t.h, (cuuint64_t)t.b};
@@ -72,7 +73,7 @@ ra_status make_tmap(const Bhsd& t, CUtensorMap* m) {
   if (sb <= 0) sb = 8;
   long long sh = t.h > 1 ? t.sh : (t.ss * t.s > 0 ? t.ss * t.s : 8);
   cuuint64_t strides[3] = {(cuuint64_t)(t.ss * 2), (cuuint64_t)(sh * 2), (cuuint64_t)(sb * 2)};
-  cuuint32_t box[4] = {64, (cuuint32_t)kTileM, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.data, dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -340,7 +341,15 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
     RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, st)));
   }
-  {
+  if (q.d == 128 && __atomic_load_n(&g_dkdv_pair, __ATOMIC_RELAXED)) {
+    CUtensorMap pq, pk, pv, pdo;  // 64-row boxes: the pair kernel loads 64 x 64 blocks
+    RA_TRY(make_tmap(q, &pq, 64));
+    RA_TRY(make_tmap(k, &pk, 64));
+    RA_TRY(make_tmap(v, &pv, 64));
+    RA_TRY(make_tmap(dout, &pdo, 64));
+    TimedLaunch tl(RA_KERNEL_BWD, st);
+    RA_TRY(cuda_status(launch_dkdv_pair(pq, pk, pv, pdo, p, st)));
+  } else {
     TimedLaunch tl(RA_KERNEL_BWD, st);
     RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 0, st)));
   }
@@ -813,6 +822,11 @@ ra_status ring_attn_set_knob(int32_t knob, int64_t value) {
   if (knob == RA_KNOB_DEBUG_FLAGS) {
     if (value < 0 || value > 1) return RA_ERR_INVALID_ARG;
     g_debug_flags = (int)value;
+    return RA_OK;
+  }
+  if (knob == RA_KNOB_DKDV_PAIR) {
+    if (value < 0 || value > 1) return RA_ERR_INVALID_ARG;
+    __atomic_store_n(&g_dkdv_pair, (int)value, __ATOMIC_RELAXED);
     return RA_OK;
   }
   return RA_ERR_INVALID_ARG;

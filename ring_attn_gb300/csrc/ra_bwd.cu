@@ -19,69 +19,18 @@
 // tile pair) is bounded by the GPU's reduction bandwidth.  The results are
 // deterministic.
 //
-// In the backward the per-element work needs no row reduction (lse and D are
-// known), so each row is split between two threads: warpgroup 1 takes columns
-// [0, 64) and warpgroup 2 columns [64, 128) of every tile row.  A thread writes
-// its bf16 results over the first 32 of its own 64 fp32 columns, so the packed
-// operand of a tile sits at TMEM columns [0, 32) and [64, 96) of the region,
-// and the 16-column K step kk of a TMEM A operand starts at column
-// pcol(kk) = 8 kk (kk < 4) or 64 + 8 (kk - 4).
-#include "ra_tiles.cuh"
+// Each tile row is split between two threads (query or key columns [0, 64) and
+// [64, 128)); ra_bwd_common.cuh describes the packed TMEM operands this gives.
+#include "ra_bwd_common.cuh"
 
 namespace ra {
 namespace {
 
-constexpr int kBox = 128 * 128;
+using bwd::kBox;
+using bwd::pcol;
+using bwd::store_rows_bf16;
+using bwd::tmem_ld64;
 constexpr int kThreads = 384;
-
-__device__ __forceinline__ uint32_t pcol(int kk) { return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4); }
-
-// 64 fp32 TMEM columns of this thread's lane into v (one wait).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
-  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-  tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 0));
-  tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + 32));
-}
-
-// The warp's 32 output row segments (lane l: N32 * 32 columns of row l, from
-// TMEM, times mul, as bf16) leave through a shared-memory slot of 32 * N32 * 64
-// bytes: each lane writes its segment there (16-byte pieces, the piece index
-// XOR the row's low bits, so the lanes spread over the banks), then the warp
-// stores whole segments with consecutive lanes on consecutive pieces.  Rows
-// [0, nvalid) are written; dst0 is row 0's segment, stride the row pitch.
-template <int N32>
-__device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul, uint8_t* slot, __nv_bfloat16* dst0,
-                                                long long stride, int nvalid) {
-  constexpr int kPieces = 4 * N32;                      // 16-byte pieces per segment
-  constexpr int kSwz = kPieces < 8 ? kPieces - 1 : 7;  // XOR mask on the piece index
-  const int lane = threadIdx.x & 31;
-  uint8_t* mine = slot + lane * kPieces * 16;
-#pragma unroll
-  for (int c = 0; c < N32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(taddr + c * 32, o);
-    tmem_ld_wait(o);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * mul, __uint_as_float(o[8 * u + 1]) * mul);
-      w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * mul, __uint_as_float(o[8 * u + 3]) * mul);
-      w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * mul, __uint_as_float(o[8 * u + 5]) * mul);
-      w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * mul, __uint_as_float(o[8 * u + 7]) * mul);
-      *reinterpret_cast<uint4*>(mine + (((c * 4 + u) ^ (lane & kSwz)) << 4)) = w;
-    }
-  }
-  __syncwarp();
-  constexpr int kRowsPer = 32 / kPieces;  // segments per warp-wide store
-  const int pc = lane % kPieces;
-#pragma unroll 1
-  for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
-    const int row = r0 + lane / kPieces;
-    const uint4 v = *reinterpret_cast<const uint4*>(slot + row * kPieces * 16 + ((pc ^ (row & kSwz)) << 4));
-    if (row < nvalid) *reinterpret_cast<uint4*>(dst0 + row * stride + pc * 8) = v;
-  }
-}
 
 // ======================================================================== dK / dV
 // Warps: 0 TMA (K, V once; Q with the query tile's -lse2 / -D, and dO, into two

@@ -210,6 +210,94 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// ------------------------------------------------------------------ CTA pairs (cta_group::2)
+// A cluster of two CTAs on two SMs runs one M = 256 MMA: each CTA holds 128
+// rows of A and half of B's N columns at the same shared-memory offsets, and
+// each CTA's tensor memory holds its 128 rows of D.  One thread of the even
+// CTA issues the MMAs; every tcgen05 instruction of such a kernel uses
+// cta_group::2 (the assembler refuses a mix).  Allocation and deallocation
+// are collective: one warp of each CTA of the pair executes them.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier anywhere in the cluster (addr from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Every thread of both CTAs: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` of every CTA in cta_mask when
+// the issuing thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// Tiled load into this CTA's shared memory whose completion (transaction
+// bytes) is signalled on an mbarrier of either CTA of the pair (bar from
+// mapa_shared).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                                 int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
+      "%4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Instruction descriptor for kind::f16: bf16 A and B, fp32 D, dense.
 // a_mn / b_mn: 0 = K-major, 1 = MN-major operand in shared memory.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
@@ -461,6 +549,68 @@ namespace ra {
 static __device__ __forceinline__ void drain_one(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
   unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > c.wait_limit_ns) {
+      record_error(c, DEV_TIMEOUT, site);
+      return;
+    }
+  }
+}
+}  // namespace ra
+
+namespace ra {
+// Bounded waits of a CTA pair: acquire at cluster scope (the barriers also
+// collect arrivals and copies from the other CTA), and a timeout raises the
+// abort flag of both CTAs (peer_abort: the other CTA's flag, from mapa_shared),
+// so that the partner leaves its loops at once instead of timing out too.
+static __device__ __forceinline__ bool wait_one_pair(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     uint32_t peer_abort, const DevCtl& c, int site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > c.wait_limit_ns) {
+        *abort_flag = 1;
+        st_shared_cluster(peer_abort, 1u);
+        record_error(c, DEV_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+}
+
+static __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                      uint32_t peer_abort, const DevCtl& c, int site) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    bool done = mbar_try_wait_cluster(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((it & 15u) == 15u) {
+      int stop = 0;
+      if (lane_id() == 0) {
+        if (*abort_flag) {
+          stop = 1;
+        } else {
+          unsigned long long now = globaltimer();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > c.wait_limit_ns) {
+            *abort_flag = 1;
+            st_shared_cluster(peer_abort, 1u);
+            record_error(c, DEV_TIMEOUT, site);
+            stop = 1;
+          }
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+static __device__ __forceinline__ void drain_one_pair(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
+  unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (globaltimer() - t0 > c.wait_limit_ns) {
       record_error(c, DEV_TIMEOUT, site);
       return;

@@ -79,6 +79,11 @@ size_t fwd_smem_bytes(int D);
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st);
 
+// The dK / dV kernel on CTA pairs (cta_group::2), head_dim 128 only.  The four
+// tensor maps have 64 x 64 boxes (64 head dims by 64 rows).
+cudaError_t launch_dkdv_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
+
 // Per query row: -D = -rowsum(dO * O) and -lse2 = -lse * log2(e), stored per
 // shard with the rows padded to stat_L (padding rows get 0 and -inf); negated so
 // that the backward adds them in packed f32x2 arithmetic.

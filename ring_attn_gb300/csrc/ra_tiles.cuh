@@ -178,7 +178,8 @@ __device__ __forceinline__ void row_key_window(const P& p, int gq, int s, int kt
   }
 }
 
-// Key rows [j0, j0 + 128) of KV shard s.
+// Key rows [j0, j0 + rows) of KV shard s (rows = 128, or 256 for the key
+// tiles of a CTA pair, whose query walk is the union of its two tiles').
 struct KRange {
   int s, j0, j_last;
   int gk_lo, gk_hi;
@@ -190,10 +191,10 @@ struct KRange {
 };
 
 template <class P>
-__device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k) {
+__device__ __forceinline__ void make_krange(const P& p, int s, int j0, KRange& k, int rows = kTileN) {
   k.s = s;
   k.j0 = j0;
-  k.j_last = min(j0 + kTileN, p.L) - 1;
+  k.j_last = min(j0 + rows, p.L) - 1;
   int sa, sz;
   ends_and_segments(p, s, j0, k.j_last, k.gk_lo, k.gk_hi, sa, sz);
   k.qry_lo = k.qry_hi = k.zb = k.zc = k.zo = 0;
