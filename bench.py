@@ -341,6 +341,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-legs", action="store_true", help="skip the contiguous-16k and stripe-128k legs")
+    ap.add_argument("--dkdv", choices=["pair", "one"], default=None,
+                    help="dK / dV kernel at head_dim 128: CTA pairs or one CTA per key tile (default: the library's)")
     ap.add_argument("--seq", type=int, default=None, help="smaller sequence length (profiling cases only)")
     ap.add_argument("--heads", type=int, default=None, help="fewer heads (profiling cases only)")
     ap.add_argument("--varlen", type=int, choices=[5, 6], default=None,
@@ -374,6 +376,8 @@ def main():
     from workload import make_qkv
 
     ra.load()
+    if args.dkdv:
+        ra.ring_attn_set_knob(ra.RA_KNOB_DKDV_PAIR, 1 if args.dkdv == "pair" else 0)
     dev = torch.device("cuda", local)
     peaks = _peaks()
     if args.varlen:

@@ -266,11 +266,11 @@ ra_status ring_attn_check_device_error(void* stream, int32_t* info);
 /* Knobs (process-wide).  RA_KNOB_WAIT_LIMIT_NS: the bounded-wait limit in ns
  * (default 4e9).  RA_KNOB_DEBUG_FLAGS: bit 0 makes the forward's TMA producer
  * skip the Q tile load, so that every consumer's bounded wait runs out: a test
- * of the timeout path that hangs nothing.  RA_KNOB_DKDV_PAIR: 1 (default) runs
- * the backward's dK / dV pass at head_dim 128 on CTA pairs (two SMs share each
+ * of the timeout path that hangs nothing.  RA_KNOB_DKDV_PAIR: 1 runs the
+ * backward's dK / dV pass at head_dim 128 on CTA pairs (two SMs share each
  * M = 256 tensor-core MMA, halving each SM's operand reads from shared memory);
- * 0 runs the one-CTA kernel, which head_dim 64 always uses.  Both give the
- * same results up to fp32 summation order. */
+ * 0 (default) runs the one-CTA kernel, which head_dim 64 always uses.  Both
+ * give the same results up to fp32 summation order. */
 typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1, RA_KNOB_DKDV_PAIR = 2 } ra_knob;
 ra_status ring_attn_set_knob(int32_t knob, int64_t value);
 
@@ -296,6 +296,14 @@ const char* ra_status_string(int32_t status);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ring_attn_version(void);
+
+/* 1 in the debug variant of the library (libringattn_dbg.so, compiled with
+ * RA_DEBUG_BOUNDS), else 0.  In that variant every kernel checks each tiled
+ * copy's coordinates, each statistics copy and each global row store against
+ * the tensors' extents before making it; a violation skips the access and
+ * records RA_ERR_DEVICE, with the site in the low byte of check_device_error's
+ * info (0x80 | site), instead of touching memory outside a tensor. */
+int32_t ring_attn_debug_bounds(void);
 
 #ifdef __cplusplus
 }

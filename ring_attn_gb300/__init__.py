@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
     "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch", "ring_attn_varlen_permute",
     "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd",
+    "ring_attn_debug_bounds",
 )
 RA_STATIC_SCRATCH_BYTES = 16 << 20
 KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
@@ -57,7 +58,13 @@ _LIB = None
 
 
 def lib_path() -> str:
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libringattn.so")
+    """libringattn.so, or the debug-bounds variant libringattn_dbg.so when
+    RA_LIB_VARIANT=debug_bounds (build it with build(debug_bounds=True))."""
+    variant = os.environ.get("RA_LIB_VARIANT", "")
+    if variant not in ("", "debug_bounds"):
+        raise ValueError(f"RA_LIB_VARIANT={variant!r}: expected 'debug_bounds' or unset")
+    name = "libringattn_dbg.so" if variant == "debug_bounds" else "libringattn.so"
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), name)
 
 
 def load():
@@ -101,6 +108,8 @@ def load():
     lib.ra_status_string.restype = ctypes.c_char_p
     lib.ring_attn_version.argtypes = []
     lib.ring_attn_version.restype = I32
+    lib.ring_attn_debug_bounds.argtypes = []
+    lib.ring_attn_debug_bounds.restype = I32
     _LIB = lib
     return lib
 

@@ -20,7 +20,7 @@ __device__ int g_dev_err[2];  // [0] error code, [1] site | block << 8
 std::mutex g_mu;
 unsigned long long g_wait_limit_ns = 4000000000ull;
 int g_debug_flags = 0;
-int g_dkdv_pair = 1;  // head_dim 128: the dK / dV pass on CTA pairs
+int g_dkdv_pair = 0;  // head_dim 128: 1 runs the dK / dV pass on CTA pairs
 int* g_err_ptr[64] = {nullptr};
 
 ra_status dev_ctl(DevCtl* c) {
@@ -242,6 +242,7 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   p.L = (int)(k.s / n_shards);
   p.r_only = rank;
   p.q_base = rank >= 0 ? rank * p.L : 0;
+  p.q_rows = (int)q.s;
   p.layout = layout;
   p.causal = causal;
   p.step = step;
@@ -310,6 +311,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.n_ktiles = (p.L + kTileN - 1) / kTileN;
   p.r_only = rank;
   p.q_base = rank >= 0 ? rank * p.L : 0;
+  p.q_rows = (int)q.s;
   p.stat_N = stat_N;
   p.stat_r0 = rank >= 0 ? rank : 0;
   p.scale = scale;
@@ -339,7 +341,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, st)));
+    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, p.ctl, st)));
   }
   if (q.d == 128 && __atomic_load_n(&g_dkdv_pair, __ATOMIC_RELAXED)) {
     CUtensorMap pq, pk, pv, pdo;  // 64-row boxes: the pair kernel loads 64 x 64 blocks
@@ -755,6 +757,7 @@ static ra_status permute_common(const ra_tensor* src, ra_tensor* dst, int32_t la
   a.inverse = inverse;
   a.cu = cu_dev;
   a.n_seqs = n_seqs;
+  RA_TRY(dev_ctl(&a.ctl));
   TimedLaunch tl(RA_KERNEL_PERMUTE, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
@@ -871,6 +874,14 @@ const char* ra_status_string(int32_t status) {
   }
 }
 
-int32_t ring_attn_version(void) { return 100; }
+int32_t ring_attn_version(void) { return 200; }
+
+int32_t ring_attn_debug_bounds(void) {
+#ifdef RA_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 }  // extern "C"

@@ -28,6 +28,7 @@ namespace {
 
 using bwd::kBox;
 using bwd::pcol;
+using bwd::stat_rows_ok;
 using bwd::store_rows_bf16;
 using bwd::tmem_ld64;
 constexpr int kThreads = 384;
@@ -151,10 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued[2] = {0, 0};
       const int krow = k.s * p.L + k.j0;
       mbar_expect_tx(BAR(E_KV_FULL), 2 * LY::kTile);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, h, b);
-        tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
-      }
+      for (int c = 0; c < D / 64; ++c)
+        if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, krow, h, b), p.ctl, 10)) {
+          tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, h, b);
+          tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
+        }
       int i = 0;
       walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
         const int st = i & 1;
@@ -165,16 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
         mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
-        bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(E_Q_FULL + st));
-        bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(E_Q_FULL + st));
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 11))
+            tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
+        if (in_bounds(stat_rows_ok(p, e0), p.ctl, 12)) {
+          bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(E_Q_FULL + st));
+          bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(E_Q_FULL + st));
+        }
         if (i >= 2 && !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)) {
           drain_one(BAR(E_Q_FULL + st), (i >> 1) & 1, p.ctl, 43);
           return false;
         }
         mbar_expect_tx(BAR(E_DO_FULL + st), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_DO_FULL + st), c * 64, qrow, h, b);
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 13))
+            tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_DO_FULL + st), c * 64, qrow, h, b);
         ++issued[st];
         ++i;
         return true;
@@ -390,11 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         const int j_w = j - lane;  // the warp's first key row
         const long long pitch = half == 0 ? p.v_ss : p.k_ss;
-        store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
-                                sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch,
-                                min(max(p.L - j_w, 0), 32));
+        const int nvalid = min(max(p.L - j_w, 0), 32);
+        const long long row_w = (long long)k.s * p.L + j_w;  // the warp's first row of dk / dv
+        if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.S), p.ctl, 14))
+          store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
+                                  sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch, nvalid);
       }
-    } else if (valid_k) {
+    } else if (valid_k && in_bounds(prow >= 0 && prow < p.S, p.ctl, 15)) {
       for (int u = 0; u < D / 8; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -537,10 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         const int qrow = r * p.L + i0 - p.q_base;
         mbar_expect_tx(BAR(F_QDO_FULL), 2 * LY::kTile);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
-          tma_load_4d(sb + LY::kDO + c * kBox, &tmDO, BAR(F_QDO_FULL), c * 64, qrow, h, b);
-        }
+        for (int c = 0; c < D / 64; ++c)
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 16)) {
+            tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
+            tma_load_4d(sb + LY::kDO + c * kBox, &tmDO, BAR(F_QDO_FULL), c * 64, qrow, h, b);
+          }
         q_issued = true;
       }
       int j = 0;
@@ -550,7 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         mbar_expect_tx(BAR(full0 + st), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, s * p.L + kt * kTileN, h, b), p.ctl, 17))
+            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
         ++issued[st];
         ++j;
         return true;
@@ -739,10 +749,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every MMA is done: the operand buffers hold the warps' row slots
         fence_proxy_async_smem();
         const int i_w = i - lane;  // the warp's first query row
-        store_rows_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, sp + (warp - 4) * (32 * D),
-                                dst - lane * p.q_ss, p.q_ss, min(max(p.L - i_w, 0), 32));
+        const int nvalid = min(max(p.L - i_w, 0), 32);
+        const long long row_w = (long long)r * p.L + i_w - p.q_base;  // the warp's first row of dq
+        if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.q_rows), p.ctl, 18))
+          store_rows_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, sp + (warp - 4) * (32 * D),
+                                  dst - lane * p.q_ss, p.q_ss, nvalid);
       }
-    } else if (valid) {
+    } else if (valid && in_bounds((long long)r * p.L + i - p.q_base < p.q_rows, p.ctl, 19)) {
       for (int u = 0; u < D / 16; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }

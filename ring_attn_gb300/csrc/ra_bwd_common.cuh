@@ -65,5 +65,12 @@ static __device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul
   }
 }
 
+// The 128 statistics rows of a query tile starting at row e0 lie inside the
+// statistics arrays and start 512-byte aligned (the bulk copies need 16).
+template <class P>
+static __device__ __forceinline__ bool stat_rows_ok(const P& p, long long e0) {
+  return e0 >= 0 && (e0 & 127) == 0 && e0 + 128 <= (long long)p.B * p.H * p.stat_N * p.stat_L;
+}
+
 }  // namespace bwd
 }  // namespace ra

@@ -15,7 +15,7 @@
 namespace ra {
 
 // ------------------------------------------------------------------ errors
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_BAD_SMEM = 7 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 6, DEV_BAD_SMEM = 7, DEV_BOUNDS = 7 };
 
 struct DevCtl {
   int* err_word;          // first error code wins (atomicCAS from 0)
@@ -30,6 +30,39 @@ __device__ __forceinline__ void record_error(const DevCtl& c, int code, int site
   if (atomicCAS(c.err_word, 0, code) == 0) {
     atomicExch(c.err_info, site | (int)((blockIdx.x + blockIdx.y * gridDim.x) << 8));
   }
+}
+
+// ------------------------------------------------------------------ debug bounds checks
+// Built with RA_DEBUG_BOUNDS (the library's debug variant), every tiled copy,
+// statistics copy and global row store first checks its coordinates against
+// the tensor's extents; a failed check records DEV_BOUNDS (RA_ERR_DEVICE)
+// with the site in the error word and skips the access (the kernel's bounded
+// waits then end the CTA).  Without the flag the checks compile away.
+#ifdef RA_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(bool ok, const DevCtl& c, int site) {
+  if (kDebugBounds && !ok) {
+    record_error(c, DEV_BOUNDS, 0x80 | site);
+    return false;
+  }
+  return true;
+}
+
+// Extents of a (b, h, rows, d) tensor as its TMA map sees it.
+struct TmaExtent {
+  int d, rows, h, b;
+};
+
+// A 64-column tiled copy starting at (c0, c1, c2, c3): 16-byte aligned column
+// start inside the row, a start row inside the tensor or at most one 128-row
+// tile past its end (that copy reads the zero fill), head and batch inside.
+__device__ __forceinline__ bool tma_coords_ok(const TmaExtent& e, int c0, int c1, int c2, int c3) {
+  return c0 >= 0 && (c0 & 63) == 0 && c0 + 64 <= e.d && c1 >= 0 && c1 < e.rows + 128 && c2 >= 0 && c2 < e.h &&
+         c3 >= 0 && c3 < e.b;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -228,20 +261,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier anywhere in the cluster (addr from mapa_shared).
+// Arrive on an mbarrier anywhere in the cluster (addr from mapa_shared).  The
+// pair kernels hand over tensor-memory contents and copy completions only,
+// which the tcgen05 fences and the barriers' own transaction accounting
+// order, so CTA-scope release suffices: cluster scope would put a memory
+// barrier into every arrival (and, on the waiting side, every poll).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 __device__ __forceinline__ void st_shared_cluster(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -558,16 +584,15 @@ static __device__ __forceinline__ void drain_one(uint32_t bar, uint32_t parity, 
 }  // namespace ra
 
 namespace ra {
-// Bounded waits of a CTA pair: acquire at cluster scope (the barriers also
-// collect arrivals and copies from the other CTA), and a timeout raises the
-// abort flag of both CTAs (peer_abort: the other CTA's flag, from mapa_shared),
-// so that the partner leaves its loops at once instead of timing out too.
+// Bounded waits of a CTA pair: a timeout raises the abort flag of both CTAs
+// (peer_abort: the other CTA's flag, from mapa_shared), so that the partner
+// leaves its loops at once instead of timing out too.
 static __device__ __forceinline__ bool wait_one_pair(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                      uint32_t peer_abort, const DevCtl& c, int site) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > c.wait_limit_ns) {
@@ -584,7 +609,7 @@ static __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t par
                                                       uint32_t peer_abort, const DevCtl& c, int site) {
   unsigned long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
-    bool done = mbar_try_wait_cluster(bar, parity);
+    bool done = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     if ((it & 15u) == 15u) {
       int stop = 0;
@@ -610,7 +635,7 @@ static __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t par
 
 static __device__ __forceinline__ void drain_one_pair(uint32_t bar, uint32_t parity, const DevCtl& c, int site) {
   unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait_cluster(bar, parity)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > c.wait_limit_ns) {
       record_error(c, DEV_TIMEOUT, site);
       return;

@@ -43,6 +43,7 @@ namespace {
 
 using bwd::kBox;
 using bwd::pcol;
+using bwd::stat_rows_ok;
 using bwd::store_rows_bf16;
 using bwd::tmem_ld64;
 
@@ -89,9 +90,12 @@ enum PairBar {
   P_TEARDOWN = 16   // each CTA
 };
 
-// The four blocks of one Q or dO stage of CTA `c` for the query tile at row qrow.
+// The four blocks of one Q or dO stage of CTA `c` for the query tile at row qrow
+// (e: the tensor's extents, for the debug bounds checks).
 __device__ __forceinline__ void load_stage(uint32_t dst, const CUtensorMap* map, uint32_t bar, int qrow, int c, int h,
-                                           int b) {
+                                           int b, const TmaExtent& e, const DevCtl& ctl) {
+  // rows qrow .. qrow + 64 and head-dim columns 0 and 64 cover all four copies
+  if (!in_bounds(tma_coords_ok(e, 0, qrow, h, b) && tma_coords_ok(e, 64, qrow + 64, h, b), ctl, 20)) return;
   tma_load_4d_pair(dst + PairLayout::kX, map, bar, 0, qrow + 64 * c, h, b);
   tma_load_4d_pair(dst + PairLayout::kX2, map, bar, 64, qrow + 64 * c, h, b);
   tma_load_4d_pair(dst + PairLayout::kY, map, bar, 64 * c, qrow, h, b);
@@ -180,11 +184,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int issued[2] = {0, 0};
         const int krow = s * p.L + j0;
         if (crank == 0) mbar_expect_tx(BAR(P_KV_FULL), 4 * LY::kTile);  // K and V of both CTAs
+        const TmaExtent ek{D, p.S, p.H, p.B}, eq{D, p.q_rows, p.H, p.B};
         for (int c = 0; c < D / 64; ++c)
-          for (int hr = 0; hr < 2; ++hr) {
-            tma_load_4d_pair(sb + LY::kK + c * kBox + hr * kSub, &tmK, LBAR(P_KV_FULL), c * 64, krow + 64 * hr, h, b);
-            tma_load_4d_pair(sb + LY::kV + c * kBox + hr * kSub, &tmV, LBAR(P_KV_FULL), c * 64, krow + 64 * hr, h, b);
-          }
+          for (int hr = 0; hr < 2; ++hr)
+            if (in_bounds(tma_coords_ok(ek, c * 64, krow + 64 * hr, h, b), p.ctl, 21)) {
+              tma_load_4d_pair(sb + LY::kK + c * kBox + hr * kSub, &tmK, LBAR(P_KV_FULL), c * 64, krow + 64 * hr, h, b);
+              tma_load_4d_pair(sb + LY::kV + c * kBox + hr * kSub, &tmV, LBAR(P_KV_FULL), c * 64, krow + 64 * hr, h, b);
+            }
         int i = 0;
         walk_q_tiles<kTileM>(p, kp, p.n_qtiles, [&](int r, int qt) {
           const int st = i & 1;
@@ -194,17 +200,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
           const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
           mbar_expect_tx(BAR(P_ST_FULL + st), 2 * 512);
-          bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(P_ST_FULL + st));
-          bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(P_ST_FULL + st));
+          if (in_bounds(stat_rows_ok(p, e0), p.ctl, 22)) {
+            bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(P_ST_FULL + st));
+            bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(P_ST_FULL + st));
+          }
           if (crank == 0) mbar_expect_tx(BAR(P_Q_FULL + st), 2 * LY::kTile);
-          load_stage(sb + LY::kQ + st * LY::kTile, &tmQ, LBAR(P_Q_FULL + st), qrow, crank, h, b);
+          load_stage(sb + LY::kQ + st * LY::kTile, &tmQ, LBAR(P_Q_FULL + st), qrow, crank, h, b, eq, p.ctl);
           if (i >= 2 && !wait_one_pair(BAR(P_DO_EMPTY + st), par, abort_flag, peer_abort, p.ctl, 82)) {
             drain_one_pair(BAR(P_ST_FULL + st), (i >> 1) & 1, p.ctl, 83);
             if (crank == 0) drain_one_pair(BAR(P_Q_FULL + st), (i >> 1) & 1, p.ctl, 83);
             return false;
           }
           if (crank == 0) mbar_expect_tx(BAR(P_DO_FULL + st), 2 * LY::kTile);
-          load_stage(sb + LY::kDO + st * LY::kTile, &tmDO, LBAR(P_DO_FULL + st), qrow, crank, h, b);
+          load_stage(sb + LY::kDO + st * LY::kTile, &tmDO, LBAR(P_DO_FULL + st), qrow, crank, h, b, eq, p.ctl);
           ++issued[st];
           ++i;
           return true;
@@ -429,11 +437,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         const int j_w = j - lane;  // the warp's first key row
         const long long pitch = half == 0 ? p.v_ss : p.k_ss;
-        store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
-                                sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch,
-                                min(max(p.L - j_w, 0), 32));
+        const int nvalid = min(max(p.L - j_w, 0), 32);
+        const long long row_w = (long long)s * p.L + j_w;  // the warp's first row of dk / dv
+        if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.S), p.ctl, 23))
+          store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
+                                  sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch, nvalid);
       }
-    } else if (valid_k) {
+    } else if (valid_k && in_bounds(prow >= 0 && prow < p.S, p.ctl, 24)) {
       for (int u = 0; u < D / 8; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }

@@ -186,8 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(BAR(B_Q_FULL), kQTiles * LY::kTile);
         for (int t = 0; t < kQTiles; ++t)
           for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + LY::kQ + t * LY::kTile + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0 + t * kTileM,
-                        h, b);
+            if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, prow0 + t * kTileM, h, b), p.ctl, 1))
+              tma_load_4d(sb + LY::kQ + t * LY::kTile + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0 + t * kTileM,
+                          h, b);
         q_issued = true;
       }
       int j = 0;
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         mbar_expect_tx(BAR(full0 + st), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, s * p.L + kt * kTileN, h, b), p.ctl, 2))
+            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
         ++issued[st];
         ++j;
         return true;
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tl + LY::kTmemS + t * 128;
     const uint32_t tO = tl + LY::kTmemO + t * 128;
     const int i = i0 + t * kTileM + row;
-    const bool valid = i < p.L;
+    bool valid = i < p.L;
     // batched: tiles classified per query tile, masks per row on partial tiles;
     // varlen: every row's key window, set up once (padding rows take the last valid row's)
     QRange qt;
@@ -401,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const long long qpos = (long long)(r * p.L + i - p.q_base);  // row of q / out / lse
     float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + qpos * p.l_ss;
+    if (valid && !in_bounds(qpos >= 0 && qpos < p.q_rows, p.ctl, 3)) valid = false;  // skip this row's stores
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(B_O_DONE), 0, abort_flag, p.ctl, 9)) {
         tc_fence_after();
@@ -475,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int R0 = 0; R0 < 32; R0 += rows_per) {
             const int R = R0 + lr;
             const uint4 val = *reinterpret_cast<const uint4*>(slot + R * nch * 16 + ((pc ^ (R & 7)) << 4));
-            if (i_w + R < p.L) {
-              const long long q_row = (long long)(r * p.L + i_w + R - p.q_base);
+            const long long q_row = (long long)(r * p.L + i_w + R - p.q_base);
+            if (i_w + R < p.L && in_bounds(q_row >= 0 && q_row < p.q_rows, p.ctl, 4)) {
               const long long e = (long long)b * p.o_sb + (long long)h * p.o_sh + q_row * p.o_ss;
               *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) + e * esz + pc * 16) = val;
             }

@@ -27,6 +27,7 @@ struct FwdParams {
   int n_seqs;
   int q_base;               // token row of q / out / lse row 0 (one rank's slice: r_only * L, else 0)
   int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
+  int q_rows;               // rows of q / out / lse: S, or L for one llama3 rank (bounds checks)
   DevCtl ctl;
 };
 
@@ -50,6 +51,7 @@ struct BwdParams {
   int q_base;               // token row of q / dO / out / dq row 0 (one rank's slice: r_only * L, else 0)
   int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
   int stat_N, stat_r0;      // the statistics hold shards [stat_r0, stat_r0 + stat_N)
+  int q_rows;               // rows of q / dO / out / dq: S, or L for one llama3 rank (bounds checks)
   DevCtl ctl;
 };
 
@@ -92,7 +94,7 @@ struct LseView {
   long long sb, sh, ss;
 };
 cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
-                           int stat_L, cudaStream_t st);
+                           int stat_L, const DevCtl& ctl, cudaStream_t st);
 
 struct MergeArgs {
   float* out_acc;        // rows x d, row stride (elements)
@@ -127,6 +129,7 @@ struct PermuteArgs {
   int vpr_total;            // vectors per row (set by the launcher)
   const int* cu;            // varlen cu_seqlens (device) or nullptr
   int n_seqs;
+  DevCtl ctl;               // error word (debug bounds checks)
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 

@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vp
         const int g = a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
                       : a.layout == LAYOUT_ZIGZAG ? vz_token(a.cu, a.n_seqs, a.N, p / L, p % L)
                                                   : p;
+        if (kDebugBounds && (g < 0 || g >= a.s)) {  // the layout map left the sequence
+          record_error(a.ctl, DEV_BOUNDS, 0x80 | 30);
+          continue;
+        }
         const long long src_pos = a.inverse ? p : g;
         const long long dst_pos = a.inverse ? g : p;
         src[u] = reinterpret_cast<const V*>(sbase + src_pos * a.src_seq_stride * a.esize);
@@ -180,66 +184,63 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
   }
 }
 
-// ------------------------------------------------------------------ backward pre / post
+// ------------------------------------------------------------------ backward preprocess
 // Per query row: -D = -sum_d dO * O and -lse2 = -lse * log2(e), stored per shard
 // with each shard's rows padded to stat_L (padding: -D = 0, -lse2 = -inf, so a
-// padded column contributes P = 0 and dS = 0).  d/8 threads per row (8 bf16
-// each); blockIdx.y walks (b, h, shard), decoded once per block, and each
-// thread handles kPreUnroll rows per turn with every load issued first.
+// padded column contributes P = 0 and dS = 0).  The statistics rows are taken
+// in order, (b, h, shard, row), kPreUnroll * rows_per_block consecutive rows
+// per block and turn (they never straddle a shard: stat_L is a multiple of
+// 128), so each turn reads contiguous runs of dO and O; d/8 threads per row (8
+// bf16 each), every load of the turn issued before the first use; one
+// persistent wave of blocks strides over the turns.
 constexpr int kPreUnroll = 4;
 
-__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* nD,
-                                                            float* nlse2, int N, int stat_L) {
+__global__ void __launch_bounds__(kThreads, 4) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* nD,
+                                                               float* nlse2, int N, int stat_L, DevCtl ctl) {
   const int tpr = dout.d / 8;  // threads per row; divides 32, so a row's threads share a warp
   const int rows_per_block = kThreads / tpr;
+  const int rows_per_turn = kPreUnroll * rows_per_block;
   const int rloc = threadIdx.x / tpr, part = threadIdx.x % tpr;
   const int L = dout.s / N;
-  const long long n_bhr = (long long)dout.b * dout.h * N;
-  const int istride = (int)gridDim.x * rows_per_block;
-  for (long long bhr = blockIdx.y; bhr < n_bhr; bhr += gridDim.y) {
+  const long long n_rows = (long long)dout.b * dout.h * N * stat_L;
+  for (long long row0 = (long long)blockIdx.x * rows_per_turn; row0 < n_rows;
+       row0 += (long long)gridDim.x * rows_per_turn) {
+    const long long bhr = row0 / stat_L;
+    const int i0 = (int)(row0 - bhr * stat_L);
     const int r = (int)(bhr % N);
     const long long bh = bhr / N;
     const long long h = bh % dout.h, b = bh / dout.h;
     const __nv_bfloat16* dsrc = reinterpret_cast<const __nv_bfloat16*>(dout.data) + b * dout.sb + h * dout.sh;
     const __nv_bfloat16* osrc = reinterpret_cast<const __nv_bfloat16*>(out.data) + b * out.sb + h * out.sh;
     const float* lsrc = lse.data + b * lse.sb + h * lse.sh;
-    // loop control follows the warp's first row, so every lane of a warp runs
-    // the same turns (the shuffle below needs them all)
-    const int wrow = rloc - rloc % (32 / tpr);
-    for (int t0 = (int)blockIdx.x * rows_per_block; t0 + wrow < stat_L; t0 += kPreUnroll * istride) {
-      const int i0 = t0 + rloc;
-      uint4 x[kPreUnroll], y[kPreUnroll];
-      float l[kPreUnroll];
-      // every load of the turn first, the row's lse included: loaded after the
-      // reduction it would add one memory latency per row to each turn
+    uint4 x[kPreUnroll], y[kPreUnroll];
+    float l[kPreUnroll];
 #pragma unroll
-      for (int u = 0; u < kPreUnroll; ++u) {
-        const int i = i0 + u * istride;
-        const bool real = i < L;
-        const long long p = (long long)r * L + i;  // layout position
-        x[u] = real ? __ldcs(reinterpret_cast<const uint4*>(dsrc + p * dout.ss) + part) : make_uint4(0, 0, 0, 0);
-        y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + p * out.ss) + part) : make_uint4(0, 0, 0, 0);
-        l[u] = real && part == 0 ? __ldcs(lsrc + p * lse.ss) : INFINITY;
+    for (int u = 0; u < kPreUnroll; ++u) {
+      const int i = i0 + u * rows_per_block + rloc;
+      const long long p = (long long)r * L + i;  // layout position
+      const bool real = i < L && in_bounds(p < dout.s, ctl, 31);
+      x[u] = real ? __ldcs(reinterpret_cast<const uint4*>(dsrc + p * dout.ss) + part) : make_uint4(0, 0, 0, 0);
+      y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + p * out.ss) + part) : make_uint4(0, 0, 0, 0);
+      l[u] = real && part == 0 ? __ldcs(lsrc + p * lse.ss) : INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kPreUnroll; ++u) {
+      const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+      const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 a2 = __bfloat1622float2(xv[k]);
+        const float2 c2 = __bfloat1622float2(yv[k]);
+        acc = fmaf(a2.x, c2.x, acc);
+        acc = fmaf(a2.y, c2.y, acc);
       }
-#pragma unroll
-      for (int u = 0; u < kPreUnroll; ++u) {
-        const int i = i0 + u * istride;
-        const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
-        const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 a2 = __bfloat1622float2(xv[k]);
-          const float2 c2 = __bfloat1622float2(yv[k]);
-          acc = fmaf(a2.x, c2.x, acc);
-          acc = fmaf(a2.y, c2.y, acc);
-        }
-        for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (part == 0 && i < stat_L) {
-          const long long row = bhr * stat_L + i;
-          nD[row] = -acc;
-          nlse2[row] = l[u] * -1.4426950408889634f;  // padding rows: +inf * -log2(e) = -inf
-        }
+      for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (part == 0) {
+        const long long row = row0 + u * rows_per_block + rloc;
+        nD[row] = -acc;
+        nlse2[row] = l[u] * -1.4426950408889634f;  // padding rows: +inf * -log2(e) = -inf
       }
     }
   }
@@ -313,15 +314,22 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
-                           int stat_L, cudaStream_t st) {
-  const int rows_per_block = kThreads / (dout.d / 8);
-  const long long n_bhr = (long long)dout.b * dout.h * N;
-  const long long gy = n_bhr < 65535 ? n_bhr : 65535;
-  long long gx = ((long long)num_sms() * 16 + gy - 1) / gy;
-  const long long need_x = (stat_L + (long long)rows_per_block * kPreUnroll - 1) / ((long long)rows_per_block * kPreUnroll);
-  if (gx > need_x) gx = need_x;
-  if (gx < 1) gx = 1;
-  bwd_pre_kernel<<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L);
+                           int stat_L, const DevCtl& ctl, cudaStream_t st) {
+  const int rows_per_turn = kPreUnroll * (kThreads / (dout.d / 8));
+  if (stat_L % rows_per_turn != 0) return cudaErrorInvalidValue;  // a turn must not straddle a shard
+  const long long turns = (long long)dout.b * dout.h * N * stat_L / rows_per_turn;
+  static int per_sm[64] = {0};  // resident blocks per SM, per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!per_sm[dev]) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_pre_kernel, kThreads, 0) != cudaSuccess || n < 1) n = 1;
+    per_sm[dev] = n;
+  }
+  long long blocks = (long long)num_sms() * per_sm[dev];  // one full wave
+  if (blocks > turns) blocks = turns;
+  if (blocks < 1) blocks = 1;
+  bwd_pre_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L, ctl);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,8 @@ def test_status_strings_and_version(lib):
     assert lib.ra_status_string(0) == b"ok"
     assert b"workspace" in lib.ra_status_string(4)
     assert lib.ra_status_string(99) == b"unknown status"
-    assert lib.ring_attn_version() == 100
+    assert lib.ring_attn_version() == 200
+    assert lib.ring_attn_debug_bounds() == 0
 
 
 def test_workspace_size(lib):
@@ -233,3 +234,25 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ra.ring_attn_fwd(x, x, x)
+
+
+def test_debug_bounds_variant_builds_and_exports_everything():
+    """The RA_DEBUG_BOUNDS build (libringattn_dbg.so) exports the same C ABI and reports itself."""
+    from ring_attn_gb300.build import build
+
+    path = build(debug_bounds=True)
+    dbg = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.ring_attn_debug_bounds.restype = ctypes.c_int32
+    assert dbg.ring_attn_debug_bounds() == 1
+
+
+def test_library_variant_selection(monkeypatch):
+    monkeypatch.setenv("RA_LIB_VARIANT", "debug_bounds")
+    assert ra.lib_path().endswith("libringattn_dbg.so")
+    monkeypatch.setenv("RA_LIB_VARIANT", "")
+    assert ra.lib_path().endswith("libringattn.so")
+    monkeypatch.setenv("RA_LIB_VARIANT", "other")
+    with pytest.raises(ValueError):
+        ra.lib_path()
