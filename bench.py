@@ -446,12 +446,11 @@ def main():
     fwd_tflops = FWD_FLOP / (fwd_ms * 1e-3) / 1e12
     peak_sus = peaks["bf16_sustained"]
     # FLOP each kernel performs: forward 2 GEMMs, dK/dV 4 GEMMs, dQ 3 GEMMs (S and dP recomputed)
+    bwd_src = ["ring_attn_gb300/csrc/ra_bwd.cu", "ring_attn_gb300/csrc/ra_bwd_common.cuh"]
     kernels = {
         "ring_fwd_kernel<128>": (fwd_ms, FWD_FLOP, ["ring_attn_gb300/csrc/ra_fwd.cu"], "ring_fwd_kernel_zigzag_h32_s64k.md"),
-        "ring_dkdv_kernel<128>": (dkdv_ms, 2.0 * FWD_FLOP, ["ring_attn_gb300/csrc/ra_bwd.cu"],
-                                  "ring_dkdv_kernel_zigzag_h32_s64k.md"),
-        "ring_dq_kernel<128>": (dq_ms, 1.5 * FWD_FLOP, ["ring_attn_gb300/csrc/ra_bwd.cu"],
-                                "ring_dq_kernel_zigzag_h32_s64k.md"),
+        "ring_dkdv_kernel<128>": (dkdv_ms, 2.0 * FWD_FLOP, bwd_src, "ring_dkdv_kernel_zigzag_h32_s64k.md"),
+        "ring_dq_kernel<128>": (dq_ms, 1.5 * FWD_FLOP, bwd_src, "ring_dq_kernel_zigzag_h32_s64k.md"),
     }
     common = ["ring_attn_gb300/csrc/ra_device.cuh", "ring_attn_gb300/csrc/ra_internal.h",
               "ring_attn_gb300/csrc/ra_tiles.cuh"]
