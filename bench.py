@@ -233,12 +233,15 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
     out = torch.empty_like(g["q"])
     lse = torch.empty((w.h, w.s), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
-    ws = torch.empty(ra.ring_attn_workspace_size(1, 1, w.h, w.s, w.d, w.n_shards), dtype=torch.uint8, device=dev)
+    # one workspace for both calls (the forward's copies are dead when the backward runs);
+    # for zigzag it holds the original-order copies the library computes in
+    ws_bytes = max(ra.ring_attn_varlen_workspace_size(op, w.s, w.h, w.d, w.layout, w.n_shards) for op in (0, 1))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     cuw = ra.CuSeqlens(cu, dev)  # host and device copies made once: the timed steps copy nothing
 
     def step():
         ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cuw, None, w.n_shards, w.causal, w.scale, out=out, lse=lse,
-                                layout=w.layout)
+                                layout=w.layout, workspace=ws)
         ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cuw, None, w.n_shards, w.causal,
                                 w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, layout=w.layout)
 
@@ -256,16 +259,20 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
     ra.ring_attn_timing_enable(True)
     for _ in range(2):
         step()
-    kt = {n: ra.ring_attn_timing_read(n) for n in ("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq")}
+    kt = {n: ra.ring_attn_timing_read(n) for n in ("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq", "permute")}
     ra.ring_attn_timing_enable(False)
     st, info = ra.ring_attn_check_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st} info {info:#x} in the varlen leg")
     tf = 2.5 * w.fwd_flops() / (ms * 1e-3) / 1e12
+    steps_timed = 2  # the per-kernel pass above
     return {"workload": f"{w.name}: h{w.h} total {w.s} d{w.d}, {w.varlen_seqs} seqs, {w.n_shards} {w.layout} shards",
             "ms_per_step": ms, "tflops": tf, "frac_of_peak": tf / peaks["bf16_sustained"],
             "frac_of_burst": tf / peaks["bf16"],
-            "kernel_ms": {n: t / max(c, 1) for n, (t, c) in kt.items()},
+            "kernel_ms": {n: t / max(c, 1) for n, (t, c) in kt.items() if n != "permute"},
+            "permute_ms_per_step": kt["permute"][0] / steps_timed,
+            "path": ("zigzag order copied to original order inside the workspace, contiguous-layout kernels, "
+                     "results copied back" if w.layout == "zigzag" else "contiguous-layout kernels"),
             "flop_convention": "fwd = sum_k 4*h*L_k^2*d/2; fwd+bwd = 2.5 x fwd"}
 
 

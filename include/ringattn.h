@@ -189,7 +189,19 @@ ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q
  *     chunk 2N-1-r of each sequence in turn, so sequence k occupies positions
  *     [cu[k]/N, cu[k+1]/N) of every shard.
  * Other layouts return RA_ERR_UNSUPPORTED; a zigzag length that is not a
- * multiple of 2N returns RA_ERR_INVALID_ARG. */
+ * multiple of 2N returns RA_ERR_INVALID_ARG.
+ * Workspace.  The forward needs none and the backward needs
+ * ring_attn_varlen_workspace_size(RA_OP_BWD, ..., RA_LAYOUT_CONTIGUOUS, N)
+ * bytes (its per-row statistics).  For RA_LAYOUT_ZIGZAG a workspace of at
+ * least ring_attn_varlen_workspace_size(op, total, h, d, RA_LAYOUT_ZIGZAG, N)
+ * bytes (256-byte aligned) makes the call run in original token order: it
+ * copies its inputs out of the zigzag order into the workspace, runs the
+ * contiguous-layout kernels there and copies the results back.  On one GPU the
+ * zigzag split is only a storage order, and with short sequences its 2N chunks
+ * put several sequences into every 128-row tile, so most of the tiles' work
+ * would be masked.  With a smaller (or no) workspace the zigzag kernels run on
+ * the zigzag order directly.  Both give the same results up to fp32 summation
+ * order. */
 ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                                const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, int32_t n_seqs,
                                int32_t max_seqlen, int32_t layout, int32_t n_shards, int32_t causal,
@@ -249,6 +261,16 @@ ra_status ring_attn_varlen_permute(const ra_tensor* x, ra_tensor* y, const int32
 ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int32_t* cu_seqlens_dev,
                                      const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
                                      int32_t seq_dim, void* stream);
+
+/* Workspace bytes of a varlen call (see the varlen calls above): RA_OP_FWD: 0
+ * for RA_LAYOUT_CONTIGUOUS, and for RA_LAYOUT_ZIGZAG the original-order copies
+ * of q, k, v and out (4 * total * h * d bf16) and lse (h * total fp32);
+ * RA_OP_BWD: the per-row statistics, plus for RA_LAYOUT_ZIGZAG the copies of
+ * dO, q, k, v, out, dk and dv (7 tensors; dq reuses out's space) and lse.
+ * Each part 256-byte aligned.  0 on bad sizes (head_dim other than 64 or 128,
+ * total not a multiple of n_shards, another layout). */
+size_t ring_attn_varlen_workspace_size(int32_t op, int64_t total, int64_t h, int64_t d, int32_t layout,
+                                       int32_t n_shards);
 
 /* Workspace bytes needed by `op` (ra_op) for (b, h, s, d) split into n_shards
  * shards; 0 for RA_OP_FWD.  RA_OP_BWD: -D = -rowsum(dO*O) and -lse*log2(e) per

@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_check_device_error", "ring_attn_set_knob", "ring_attn_timing_enable", "ring_attn_timing_read",
     "ra_status_string", "ring_attn_version", "ring_attn_bwd_static_scratch", "ring_attn_varlen_permute",
     "ring_attn_varlen_unpermute", "ring_attn_llama3_varlen_fwd", "ring_attn_llama3_varlen_bwd",
-    "ring_attn_debug_bounds",
+    "ring_attn_debug_bounds", "ring_attn_varlen_workspace_size",
 )
 RA_STATIC_SCRATCH_BYTES = 16 << 20
 KERNELS = {"fwd": 0, "bwd_dkdv": 1, "bwd_pre": 2, "bwd_dq": 3, "permute": 4, "lse_merge": 5}
@@ -104,6 +104,8 @@ def load():
         f.restype = I32
     lib.ring_attn_workspace_size.argtypes = [I32, I64, I64, I64, I64, I32]
     lib.ring_attn_workspace_size.restype = SZ
+    lib.ring_attn_varlen_workspace_size.argtypes = [I32, I64, I64, I64, I32, I32]
+    lib.ring_attn_varlen_workspace_size.restype = SZ
     lib.ra_status_string.argtypes = [I32]
     lib.ra_status_string.restype = ctypes.c_char_p
     lib.ring_attn_version.argtypes = []
@@ -206,6 +208,19 @@ def ring_attn_workspace_size(op, b, h, s, d, n_shards=1) -> int:
     return int(load().ring_attn_workspace_size(int(op), int(b), int(h), int(s), int(d), int(n_shards)))
 
 
+def ring_attn_varlen_workspace_size(op, total, h, d, layout="contiguous", n_shards=1) -> int:
+    """Bytes of a varlen call's workspace (for zigzag: the original-order copies, see the C header)."""
+    return int(load().ring_attn_varlen_workspace_size(int(op), int(total), int(h), int(d), _layout(layout),
+                                                      int(n_shards)))
+
+
+def _ws_arg(workspace):
+    """(pointer, bytes) of an optional workspace tensor."""
+    if workspace is None:
+        return None, 0
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
 def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
                   dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Gradients (dq, dk, dv), bf16, layout order."""
@@ -283,10 +298,13 @@ def _cu_pair(cu_seqlens, device):
 
 
 def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
-                         out=None, lse=None, stream=None, layout="contiguous"):
+                         out=None, lse=None, stream=None, layout="contiguous", workspace=None):
     """Packed sequences, one cu_seqlens.  q, k, v: (total, h, d) or (h, total, d) bf16 in
     layout order ("contiguous" slices of the packed buffer, or "zigzag" per sequence).
 
+    workspace: None allocates what ring_attn_varlen_workspace_size asks for (for
+    zigzag, the original-order copies the library computes in); pass a tensor to
+    reuse one (an empty tensor runs the zigzag kernels directly).
     Returns (out like q, lse (h, total) fp32)."""
     lib = load()
     host, dev = _cu_pair(cu_seqlens, q.device)
@@ -298,11 +316,15 @@ def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causa
     d = q.shape[2]
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((h, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        need = ring_attn_varlen_workspace_size(RA_OP_FWD, total, h, d, layout, n_shards)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    wp, wb = _ws_arg(workspace)
     tq, tk, tv, to, tl = _t(q), _t(k), _t(v), _t(out), _t(lse)
     _check(lib.ring_attn_varlen_fwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()), n,
                                     int(max_seqlen), _layout(layout), int(n_shards), int(bool(causal)),
-                                    _scale(softmax_scale, d), ctypes.byref(to), ctypes.byref(tl), None, 0,
+                                    _scale(softmax_scale, d), ctypes.byref(to), ctypes.byref(tl), wp, wb,
                                     _stream(stream)),
            "ring_attn_varlen_fwd")
     return out, lse
@@ -322,8 +344,8 @@ def ring_attn_varlen_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seqlen=None, n
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws_bytes = ring_attn_workspace_size(RA_OP_BWD, 1, h, total, d, n_shards)
     if workspace is None:
+        ws_bytes = ring_attn_varlen_workspace_size(RA_OP_BWD, total, h, d, layout, n_shards)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ts = [_t(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
     r = [ctypes.byref(x) for x in ts]

@@ -393,6 +393,66 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
   return RA_OK;
 }
 
+// ---------------------------------------------------------------- zigzag varlen in original order
+// On one GPU the zigzag split of every sequence is only a storage order.  With
+// a large enough caller workspace the zigzag varlen calls un-permute their
+// inputs into it, run the contiguous-layout kernels (tiles then hold whole
+// runs of one sequence instead of the 2N short chunks of several), and permute
+// the outputs back.
+size_t zz_tensor_bytes(long long total, long long h, long long d) { return round256((size_t)total * h * d * 2); }
+size_t zz_lse_bytes(long long total, long long h) { return round256((size_t)total * h * 4); }
+// forward: q, k, v, out in original order (h, total, d), lse (h, total)
+size_t zz_fwd_bytes(long long total, long long h, long long d) {
+  return 4 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h);
+}
+// backward: the statistics, then dO, q, k, v, out (whose space dq reuses once
+// D = rowsum(dO * out) is taken), dk, dv, and lse
+size_t zz_bwd_bytes(long long total, long long h, long long d, int n_shards) {
+  return bwd_ws_bytes(1, h, total, n_shards) + 7 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h);
+}
+
+// A contiguous (h, total, d) bf16 view at p.
+Bhsd zz_view(void* p, long long total, long long h, long long d) {
+  return Bhsd{p, 1, h, total, d, 0, total * d, d};
+}
+
+// Permutes one (1, h, total, d) view (or an (h, total) fp32 lse when d == 0)
+// between zigzag layout order and original order: inverse = 1 reads layout
+// order (src) and writes original order (dst).
+ra_status zz_permute(const void* src, long long s_sh, long long s_ss, void* dst, long long d_sh, long long d_ss,
+                     long long h, long long total, long long d, int inverse, const int32_t* cu_dev, int32_t n_seqs,
+                     int32_t n_shards, cudaStream_t st) {
+  PermuteArgs a;
+  memset(&a, 0, sizeof(a));
+  a.src = src;
+  a.dst = dst;
+  a.esize = d > 0 ? 2 : 4;
+  a.inner = d > 0 ? d : 1;
+  for (int i = 0; i < 3; ++i) a.outer_shape[i] = 1;
+  a.outer_shape[2] = h;
+  a.src_outer_stride[2] = s_sh;
+  a.dst_outer_stride[2] = d_sh;
+  a.n_outer = h;
+  a.src_seq_stride = s_ss;
+  a.dst_seq_stride = d_ss;
+  a.s = (int)total;
+  a.layout = RA_LAYOUT_ZIGZAG;
+  a.N = n_shards;
+  a.inverse = inverse;
+  a.cu = cu_dev;
+  a.n_seqs = n_seqs;
+  RA_TRY(dev_ctl(&a.ctl));
+  TimedLaunch tl(RA_KERNEL_PERMUTE, st);
+  return cuda_status(launch_permute(a, st));
+}
+
+ra_status zz_in(const Bhsd& x, void* dst, const int32_t* cu, int32_t n, int32_t N, cudaStream_t st) {
+  return zz_permute(x.data, x.sh, x.ss, dst, x.s * x.d, x.d, x.h, x.s, x.d, 1, cu, n, N, st);
+}
+ra_status zz_out(const void* src, const Bhsd& x, const int32_t* cu, int32_t n, int32_t N, cudaStream_t st) {
+  return zz_permute(src, x.s * x.d, x.d, x.data, x.sh, x.ss, x.h, x.s, x.d, 0, cu, n, N, st);
+}
+
 }  // namespace
 
 // Statistics of ring_attn_bwd_static_scratch (-D, then -lse * log2(e)).  The
@@ -598,8 +658,6 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
                                int32_t max_seqlen, int32_t layout, int32_t n_shards, int32_t causal,
                                float softmax_scale, ra_tensor* out, ra_tensor* lse, void* workspace,
                                size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   long long total = 0;
   RA_TRY(check_cu(cu_seqlens_dev, cu_seqlens_host, n_seqs, max_seqlen, &total));
   RA_TRY(check_varlen_layout(layout, n_shards, cu_seqlens_host, n_seqs));
@@ -610,6 +668,27 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
   RA_TRY(check_thd(out, total, &vo));
   long long lsb, lsh, lss;
   RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
+  if (layout == RA_LAYOUT_ZIGZAG && workspace && workspace_bytes >= zz_fwd_bytes(total, vq.h, vq.d)) {
+    // original-order path: the same checks as the kernels' before any launch
+    if (!same_shape(vq, vk) || !same_shape(vq, vv) || !same_shape(vq, vo)) return RA_ERR_INVALID_ARG;
+    if (vq.d != 64 && vq.d != 128) return RA_ERR_UNSUPPORTED;
+    RA_TRY(check_scale(softmax_scale));
+    if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return RA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(workspace);
+    const size_t T = zz_tensor_bytes(total, vq.h, vq.d);
+    const Bhsd q2 = zz_view(w, total, vq.h, vq.d), k2 = zz_view(w + T, total, vq.h, vq.d),
+               v2 = zz_view(w + 2 * T, total, vq.h, vq.d), o2 = zz_view(w + 3 * T, total, vq.h, vq.d);
+    float* l2 = reinterpret_cast<float*>(w + 4 * T);
+    RA_TRY(zz_in(vq, q2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vk, k2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vv, v2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(fwd_common(q2, k2, v2, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, o2, 0, l2, 0, total, 1,
+                      cu_seqlens_dev, n_seqs, stream));
+    RA_TRY(zz_out(o2.data, vo, cu_seqlens_dev, n_seqs, n_shards, st));
+    return zz_permute(l2, total, 1, lse->data, lsh, lss, vq.h, total, 0, 0, cu_seqlens_dev, n_seqs, n_shards, st);
+  }
   return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, -1, vo, 0,
                     static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream);
 }
@@ -633,6 +712,31 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
   RA_TRY(check_thd(dv, total, &vdv));
   long long lsb, lsh, lss;
   RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
+  if (layout == RA_LAYOUT_ZIGZAG && workspace && workspace_bytes >= zz_bwd_bytes(total, vq.h, vq.d, n_shards)) {
+    // original-order path: the same checks as the kernels' before any launch
+    RA_TRY(bwd_check_args(vdo, vq, vk, vv, vo, layout, n_shards, causal, softmax_scale, vdq, vdk, vdv, -1));
+    if (!aligned(workspace, 256)) return RA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t SB = bwd_ws_bytes(1, vq.h, total, n_shards), T = zz_tensor_bytes(total, vq.h, vq.d);
+    char* w = static_cast<char*>(workspace) + SB;
+    const long long h = vq.h, d = vq.d;
+    const Bhsd do2 = zz_view(w, total, h, d), q2 = zz_view(w + T, total, h, d), k2 = zz_view(w + 2 * T, total, h, d),
+               v2 = zz_view(w + 3 * T, total, h, d), o2 = zz_view(w + 4 * T, total, h, d),
+               dk2 = zz_view(w + 5 * T, total, h, d), dv2 = zz_view(w + 6 * T, total, h, d);
+    float* l2 = reinterpret_cast<float*>(w + 7 * T);
+    const Bhsd& dq2 = o2;  // out is read only by the preprocess, which runs before the dQ kernel writes
+    RA_TRY(zz_in(vdo, do2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vq, q2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vk, k2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vv, v2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_in(vo, o2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_permute(lse->data, lsh, lss, l2, total, 1, h, total, 0, 1, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(bwd_common(do2, q2, k2, v2, o2, l2, 0, total, 1, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale,
+                      dq2, dk2, dv2, workspace, SB, cu_seqlens_dev, n_seqs, stream));
+    RA_TRY(zz_out(dq2.data, vdq, cu_seqlens_dev, n_seqs, n_shards, st));
+    RA_TRY(zz_out(dk2.data, vdk, cu_seqlens_dev, n_seqs, n_shards, st));
+    return zz_out(dv2.data, vdv, cu_seqlens_dev, n_seqs, n_shards, st);
+  }
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,
                     stream);
@@ -792,6 +896,15 @@ ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int
                                      const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t layout, int32_t n_shards,
                                      int32_t seq_dim, void* stream) {
   return varlen_permute_common(y, x, cu_seqlens_dev, cu_seqlens_host, n_seqs, layout, n_shards, seq_dim, 1, stream);
+}
+
+size_t ring_attn_varlen_workspace_size(int32_t op, int64_t total, int64_t h, int64_t d, int32_t layout,
+                                       int32_t n_shards) {
+  if (total < 1 || h < 1 || (d != 64 && d != 128) || n_shards < 1 || total % n_shards) return 0;
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG) return 0;
+  if (op == RA_OP_FWD) return layout == RA_LAYOUT_ZIGZAG ? zz_fwd_bytes(total, h, d) : 0;
+  if (op != RA_OP_BWD) return 0;
+  return layout == RA_LAYOUT_ZIGZAG ? zz_bwd_bytes(total, h, d, n_shards) : bwd_ws_bytes(1, h, total, n_shards);
 }
 
 size_t ring_attn_workspace_size(int32_t op, int64_t b, int64_t h, int64_t s, int64_t d, int32_t n_shards) {

@@ -256,3 +256,18 @@ def test_library_variant_selection(monkeypatch):
     monkeypatch.setenv("RA_LIB_VARIANT", "other")
     with pytest.raises(ValueError):
         ra.lib_path()
+
+
+def test_varlen_workspace_sizes(lib):
+    T = lambda total, h, d: -(-total * h * d * 2 // 256) * 256  # noqa: E731
+    Lb = lambda total, h: -(-total * h * 4 // 256) * 256  # noqa: E731
+    total, h, d, n = 131072, 32, 128, 8
+    stats = lib.ring_attn_workspace_size(1, 1, h, total, d, n)
+    assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 0, n) == 0
+    assert lib.ring_attn_varlen_workspace_size(1, total, h, d, 0, n) == stats
+    assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 1, n) == 4 * T(total, h, d) + Lb(total, h)
+    assert lib.ring_attn_varlen_workspace_size(1, total, h, d, 1, n) == stats + 7 * T(total, h, d) + Lb(total, h)
+    assert lib.ring_attn_varlen_workspace_size(0, total, h, 96, 1, n) == 0    # head_dim
+    assert lib.ring_attn_varlen_workspace_size(0, total + 1, h, d, 1, n) == 0  # total % n_shards
+    assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 2, n) == 0     # stripe varlen
+    assert ra.ring_attn_varlen_workspace_size(1, total, h, d, "zigzag", n) == stats + 7 * T(total, h, d) + Lb(total, h)

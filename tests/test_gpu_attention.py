@@ -216,16 +216,28 @@ def test_varlen_zigzag_permute_bit_exact(ra, lens, n):
 ])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d):
+@pytest.mark.parametrize("path", ["original_order", "direct"])
+def test_varlen_zigzag_fwd_bwd(ra, lens, n, causal, d, path):
+    """Both ways a zigzag varlen call runs: in original token order inside the
+    workspace (the binding's default), and on the zigzag order directly (a
+    workspace too small for the copies)."""
     h = 2
     cu = cu_seqlens(lens)
-    x = make_qkv(1, h, cu[-1], d, 300 + len(lens) + n, with_do=True)
+    total = int(cu[-1])
+    x = make_qkv(1, h, total, d, 300 + len(lens) + n, with_do=True)
     scale = d ** -0.5
     g = {k: ra.ring_attn_varlen_permute(v[0].transpose(0, 1).contiguous().cuda(), cu, "zigzag", n, seq_dim=0)
          for k, v in x.items()}
-    out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, causal, scale, layout="zigzag")
+    if path == "direct":
+        ws_f = torch.empty(0, dtype=torch.uint8, device="cuda")
+        ws_b = torch.empty(ra.ring_attn_varlen_workspace_size(1, total, h, d, "contiguous", n), dtype=torch.uint8,
+                           device="cuda")
+    else:
+        ws_f = ws_b = None
+    out, lse = ra.ring_attn_varlen_fwd(g["q"], g["k"], g["v"], cu, None, n, causal, scale, layout="zigzag",
+                                       workspace=ws_f)
     dq, dk, dv = ra.ring_attn_varlen_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, cu, None, n, causal, scale,
-                                         layout="zigzag")
+                                         layout="zigzag", workspace=ws_b)
     check_no_device_error(ra)
     ref_o, ref_l = oracle.attention_fwd(x["q"], x["k"], x["v"], scale, causal, cu_seqlens=cu)
     ref_g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, cu_seqlens=cu)
