@@ -266,7 +266,8 @@ ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int
  * for RA_LAYOUT_CONTIGUOUS, and for RA_LAYOUT_ZIGZAG the original-order copies
  * of q, k, v and out (4 * total * h * d bf16) and lse (h * total fp32);
  * RA_OP_BWD: the per-row statistics, plus for RA_LAYOUT_ZIGZAG the copies of
- * dO, q, k, v, out, dk and dv (7 tensors; dq reuses out's space) and lse.
+ * dO, q, k, v, out, dk and dv (7 tensors; dq reuses out's space) and lse;
+ * zigzag also takes total int32 for the layout-to-token map of the copies.
  * Each part 256-byte aligned.  0 on bad sizes (head_dim other than 64 or 128,
  * total not a multiple of n_shards, another layout). */
 size_t ring_attn_varlen_workspace_size(int32_t op, int64_t total, int64_t h, int64_t d, int32_t layout,

@@ -401,14 +401,16 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
 // the outputs back.
 size_t zz_tensor_bytes(long long total, long long h, long long d) { return round256((size_t)total * h * d * 2); }
 size_t zz_lse_bytes(long long total, long long h) { return round256((size_t)total * h * 4); }
-// forward: q, k, v, out in original order (h, total, d), lse (h, total)
+size_t zz_map_bytes(long long total) { return round256((size_t)total * 4); }
+// forward: q, k, v, out in original order (h, total, d), lse (h, total), the token map
 size_t zz_fwd_bytes(long long total, long long h, long long d) {
-  return 4 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h);
+  return 4 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) + zz_map_bytes(total);
 }
 // backward: the statistics, then dO, q, k, v, out (whose space dq reuses once
-// D = rowsum(dO * out) is taken), dk, dv, and lse
+// D = rowsum(dO * out) is taken), dk, dv, lse and the token map
 size_t zz_bwd_bytes(long long total, long long h, long long d, int n_shards) {
-  return bwd_ws_bytes(1, h, total, n_shards) + 7 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h);
+  return bwd_ws_bytes(1, h, total, n_shards) + 7 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) +
+         zz_map_bytes(total);
 }
 
 // A contiguous (h, total, d) bf16 view at p.
@@ -421,7 +423,7 @@ Bhsd zz_view(void* p, long long total, long long h, long long d) {
 // order (src) and writes original order (dst).
 ra_status zz_permute(const void* src, long long s_sh, long long s_ss, void* dst, long long d_sh, long long d_ss,
                      long long h, long long total, long long d, int inverse, const int32_t* cu_dev, int32_t n_seqs,
-                     int32_t n_shards, cudaStream_t st) {
+                     int32_t n_shards, const int* gmap, cudaStream_t st) {
   PermuteArgs a;
   memset(&a, 0, sizeof(a));
   a.src = src;
@@ -441,16 +443,29 @@ ra_status zz_permute(const void* src, long long s_sh, long long s_ss, void* dst,
   a.inverse = inverse;
   a.cu = cu_dev;
   a.n_seqs = n_seqs;
+  a.gmap = gmap;
   RA_TRY(dev_ctl(&a.ctl));
   TimedLaunch tl(RA_KERNEL_PERMUTE, st);
   return cuda_status(launch_permute(a, st));
 }
 
-ra_status zz_in(const Bhsd& x, void* dst, const int32_t* cu, int32_t n, int32_t N, cudaStream_t st) {
-  return zz_permute(x.data, x.sh, x.ss, dst, x.s * x.d, x.d, x.h, x.s, x.d, 1, cu, n, N, st);
+// The copies of one call share the token map, computed once into the workspace.
+struct ZzCtx {
+  const int32_t* cu;
+  int32_t n, N;
+  const int* map;
+  cudaStream_t st;
+};
+ra_status zz_map(ZzCtx& z, void* map, long long total) {
+  z.map = static_cast<const int*>(map);
+  TimedLaunch tl(RA_KERNEL_PERMUTE, z.st);
+  return cuda_status(launch_zigzag_varlen_map(z.cu, z.n, z.N, (int)total, static_cast<int*>(map), z.st));
 }
-ra_status zz_out(const void* src, const Bhsd& x, const int32_t* cu, int32_t n, int32_t N, cudaStream_t st) {
-  return zz_permute(src, x.s * x.d, x.d, x.data, x.sh, x.ss, x.h, x.s, x.d, 0, cu, n, N, st);
+ra_status zz_in(const ZzCtx& z, const Bhsd& x, void* dst) {
+  return zz_permute(x.data, x.sh, x.ss, dst, x.s * x.d, x.d, x.h, x.s, x.d, 1, z.cu, z.n, z.N, z.map, z.st);
+}
+ra_status zz_out(const ZzCtx& z, const void* src, const Bhsd& x) {
+  return zz_permute(src, x.s * x.d, x.d, x.data, x.sh, x.ss, x.h, x.s, x.d, 0, z.cu, z.n, z.N, z.map, z.st);
 }
 
 }  // namespace
@@ -681,13 +696,15 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
     const Bhsd q2 = zz_view(w, total, vq.h, vq.d), k2 = zz_view(w + T, total, vq.h, vq.d),
                v2 = zz_view(w + 2 * T, total, vq.h, vq.d), o2 = zz_view(w + 3 * T, total, vq.h, vq.d);
     float* l2 = reinterpret_cast<float*>(w + 4 * T);
-    RA_TRY(zz_in(vq, q2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vk, k2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vv, v2.data, cu_seqlens_dev, n_seqs, n_shards, st));
+    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, nullptr, st};
+    RA_TRY(zz_map(z, w + 4 * T + zz_lse_bytes(total, vq.h), total));
+    RA_TRY(zz_in(z, vq, q2.data));
+    RA_TRY(zz_in(z, vk, k2.data));
+    RA_TRY(zz_in(z, vv, v2.data));
     RA_TRY(fwd_common(q2, k2, v2, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, o2, 0, l2, 0, total, 1,
                       cu_seqlens_dev, n_seqs, stream));
-    RA_TRY(zz_out(o2.data, vo, cu_seqlens_dev, n_seqs, n_shards, st));
-    return zz_permute(l2, total, 1, lse->data, lsh, lss, vq.h, total, 0, 0, cu_seqlens_dev, n_seqs, n_shards, st);
+    RA_TRY(zz_out(z, o2.data, vo));
+    return zz_permute(l2, total, 1, lse->data, lsh, lss, vq.h, total, 0, 0, z.cu, z.n, z.N, z.map, st);
   }
   return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, -1, vo, 0,
                     static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream);
@@ -725,17 +742,19 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
                dk2 = zz_view(w + 5 * T, total, h, d), dv2 = zz_view(w + 6 * T, total, h, d);
     float* l2 = reinterpret_cast<float*>(w + 7 * T);
     const Bhsd& dq2 = o2;  // out is read only by the preprocess, which runs before the dQ kernel writes
-    RA_TRY(zz_in(vdo, do2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vq, q2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vk, k2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vv, v2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_in(vo, o2.data, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_permute(lse->data, lsh, lss, l2, total, 1, h, total, 0, 1, cu_seqlens_dev, n_seqs, n_shards, st));
+    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, nullptr, st};
+    RA_TRY(zz_map(z, w + 7 * T + zz_lse_bytes(total, h), total));
+    RA_TRY(zz_in(z, vdo, do2.data));
+    RA_TRY(zz_in(z, vq, q2.data));
+    RA_TRY(zz_in(z, vk, k2.data));
+    RA_TRY(zz_in(z, vv, v2.data));
+    RA_TRY(zz_in(z, vo, o2.data));
+    RA_TRY(zz_permute(lse->data, lsh, lss, l2, total, 1, h, total, 0, 1, z.cu, z.n, z.N, z.map, st));
     RA_TRY(bwd_common(do2, q2, k2, v2, o2, l2, 0, total, 1, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale,
                       dq2, dk2, dv2, workspace, SB, cu_seqlens_dev, n_seqs, stream));
-    RA_TRY(zz_out(dq2.data, vdq, cu_seqlens_dev, n_seqs, n_shards, st));
-    RA_TRY(zz_out(dk2.data, vdk, cu_seqlens_dev, n_seqs, n_shards, st));
-    return zz_out(dv2.data, vdv, cu_seqlens_dev, n_seqs, n_shards, st);
+    RA_TRY(zz_out(z, dq2.data, vdq));
+    RA_TRY(zz_out(z, dk2.data, vdk));
+    return zz_out(z, dv2.data, vdv);
   }
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,

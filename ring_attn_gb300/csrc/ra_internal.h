@@ -129,9 +129,14 @@ struct PermuteArgs {
   int vpr_total;            // vectors per row (set by the launcher)
   const int* cu;            // varlen cu_seqlens (device) or nullptr
   int n_seqs;
+  const int* gmap;          // optional: gmap[p] = original token at layout position p (replaces the search)
   DevCtl ctl;               // error word (debug bounds checks)
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
+
+// map[p] = original token at layout position p of the zigzag varlen split of
+// one packed buffer of `total` tokens (N shards, cu_seqlens with n_seqs entries + 1).
+cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, cudaStream_t st);
 
 int num_sms();
 

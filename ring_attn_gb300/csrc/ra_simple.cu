@@ -50,7 +50,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(PermuteArgs a, int vp
         dst[u] = nullptr;
         if (p >= a.s) continue;
         // original token at layout position p
-        const int g = a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
+        const int g = a.gmap != nullptr ? __ldg(a.gmap + p)
+                      : a.cu == nullptr ? token_of(a.layout, a.N, L, p / L, p % L)
                       : a.layout == LAYOUT_ZIGZAG ? vz_token(a.cu, a.n_seqs, a.N, p / L, p % L)
                                                   : p;
         if (kDebugBounds && (g < 0 || g >= a.s)) {  // the layout map left the sequence
@@ -246,7 +247,21 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_pre_kernel(View4 dout, View4 
   }
 }
 
+// One thread per layout position: the search of cu_seqlens that the permute
+// kernel would repeat for every row of every tensor is done once per call.
+__global__ void __launch_bounds__(kThreads) zigzag_varlen_map_kernel(const int* cu, int n_seqs, int N, int L, int total,
+                                                                     int* map) {
+  for (int p = blockIdx.x * kThreads + threadIdx.x; p < total; p += gridDim.x * kThreads)
+    map[p] = vz_token(cu, n_seqs, N, p / L, p % L);
+}
+
 }  // namespace
+
+cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, cudaStream_t st) {
+  if (N < 1 || total < 1 || total % N) return cudaErrorInvalidValue;
+  zigzag_varlen_map_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(cu, n_seqs, N, total / N, total, map);
+  return cudaGetLastError();
+}
 
 int num_sms() {
   static int cached[64] = {0};

@@ -265,9 +265,11 @@ def test_varlen_workspace_sizes(lib):
     stats = lib.ring_attn_workspace_size(1, 1, h, total, d, n)
     assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 0, n) == 0
     assert lib.ring_attn_varlen_workspace_size(1, total, h, d, 0, n) == stats
-    assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 1, n) == 4 * T(total, h, d) + Lb(total, h)
-    assert lib.ring_attn_varlen_workspace_size(1, total, h, d, 1, n) == stats + 7 * T(total, h, d) + Lb(total, h)
+    M = Lb(total, 1)  # the token map: total int32
+    assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 1, n) == 4 * T(total, h, d) + Lb(total, h) + M
+    assert lib.ring_attn_varlen_workspace_size(1, total, h, d, 1, n) == stats + 7 * T(total, h, d) + Lb(total, h) + M
     assert lib.ring_attn_varlen_workspace_size(0, total, h, 96, 1, n) == 0    # head_dim
     assert lib.ring_attn_varlen_workspace_size(0, total + 1, h, d, 1, n) == 0  # total % n_shards
     assert lib.ring_attn_varlen_workspace_size(0, total, h, d, 2, n) == 0     # stripe varlen
-    assert ra.ring_attn_varlen_workspace_size(1, total, h, d, "zigzag", n) == stats + 7 * T(total, h, d) + Lb(total, h)
+    assert ra.ring_attn_varlen_workspace_size(1, total, h, d, "zigzag", n) == lib.ring_attn_varlen_workspace_size(
+        1, total, h, d, 1, n)
