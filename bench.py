@@ -271,8 +271,8 @@ def _varlen_leg(ra, torch, wid, peaks, dev, steps=5, warmup=3, heads=None):
             "frac_of_burst": tf / peaks["bf16"],
             "kernel_ms": {n: t / max(c, 1) for n, (t, c) in kt.items() if n != "permute"},
             "permute_ms_per_step": kt["permute"][0] / steps_timed,
-            "path": ("zigzag order copied to original order inside the workspace, contiguous-layout kernels, "
-                     "results copied back" if w.layout == "zigzag" else "contiguous-layout kernels"),
+            "path": ("inputs copied from zigzag to original order inside the workspace, contiguous-layout kernels "
+                     "writing their results in zigzag order" if w.layout == "zigzag" else "contiguous-layout kernels"),
             "flop_convention": "fwd = sum_k 4*h*L_k^2*d/2; fwd+bwd = 2.5 x fwd"}
 
 

@@ -221,7 +221,8 @@ ra_status bwd_check_args(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const B
 // rows (the contiguous slice [rank*L, (rank+1)*L)), k and v all S rows.
 ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout, int32_t n_shards, int32_t causal,
                      float scale, int32_t step, const Bhsd& o, int out_f32, float* lse, long long lsb, long long lsh,
-                     long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1) {
+                     long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1,
+                     const int* row_map = nullptr) {
   if (!same_shape(k, v) || !same_shape(q, o)) return RA_ERR_INVALID_ARG;
   if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
   if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
@@ -243,6 +244,7 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   p.r_only = rank;
   p.q_base = rank >= 0 ? rank * p.L : 0;
   p.q_rows = (int)q.s;
+  p.row_map = row_map;
   p.layout = layout;
   p.causal = causal;
   p.step = step;
@@ -285,7 +287,8 @@ size_t bwd_ws_bytes(long long b, long long h, long long s, int n_shards) {
 ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd& v, const Bhsd& out,
                      const float* lse, long long lsb, long long lsh, long long lss, int32_t layout, int32_t n_shards,
                      int32_t causal, float scale, const Bhsd& dq, const Bhsd& dk, const Bhsd& dv, void* ws,
-                     size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1) {
+                     size_t ws_bytes, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1,
+                     const int* row_map = nullptr) {
   RA_TRY(bwd_check_args(dout, q, k, v, out, layout, n_shards, causal, scale, dq, dk, dv, rank));
   const int stat_N = rank >= 0 ? 1 : n_shards;  // shards whose rows the statistics hold
   if (!ws || !aligned(ws, 256) || ws_bytes < bwd_ws_bytes(q.b, q.h, q.s, stat_N)) return RA_ERR_WORKSPACE;
@@ -312,6 +315,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   p.r_only = rank;
   p.q_base = rank >= 0 ? rank * p.L : 0;
   p.q_rows = (int)q.s;
+  p.row_map = row_map;
   p.stat_N = stat_N;
   p.stat_r0 = rank >= 0 ? rank : 0;
   p.scale = scale;
@@ -395,22 +399,24 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
 
 // ---------------------------------------------------------------- zigzag varlen in original order
 // On one GPU the zigzag split of every sequence is only a storage order.  With
-// a large enough caller workspace the zigzag varlen calls un-permute their
-// inputs into it, run the contiguous-layout kernels (tiles then hold whole
-// runs of one sequence instead of the 2N short chunks of several), and permute
-// the outputs back.
+// a large enough caller workspace the zigzag varlen calls copy their inputs
+// into it in original order and run the contiguous-layout kernels there (tiles
+// then hold whole runs of one sequence instead of the 2N short chunks of
+// several), which write each output row straight to its row of the caller's
+// zigzag order through the inverse token map.
 size_t zz_tensor_bytes(long long total, long long h, long long d) { return round256((size_t)total * h * d * 2); }
 size_t zz_lse_bytes(long long total, long long h) { return round256((size_t)total * h * 4); }
 size_t zz_map_bytes(long long total) { return round256((size_t)total * 4); }
-// forward: q, k, v, out in original order (h, total, d), lse (h, total), the token map
+// The outputs are written straight into the caller's layout-order rows (the
+// kernels take the inverse map), so only inputs are copied.
+// forward: q, k, v in original order (h, total, d), the map and its inverse
 size_t zz_fwd_bytes(long long total, long long h, long long d) {
-  return 4 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) + zz_map_bytes(total);
+  return 3 * zz_tensor_bytes(total, h, d) + 2 * zz_map_bytes(total);
 }
-// backward: the statistics, then dO, q, k, v, out (whose space dq reuses once
-// D = rowsum(dO * out) is taken), dk, dv, lse and the token map
+// backward: the statistics, then dO, q, k, v, out, lse, the map and its inverse
 size_t zz_bwd_bytes(long long total, long long h, long long d, int n_shards) {
-  return bwd_ws_bytes(1, h, total, n_shards) + 7 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) +
-         zz_map_bytes(total);
+  return bwd_ws_bytes(1, h, total, n_shards) + 5 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) +
+         2 * zz_map_bytes(total);
 }
 
 // A contiguous (h, total, d) bf16 view at p.
@@ -453,19 +459,20 @@ ra_status zz_permute(const void* src, long long s_sh, long long s_ss, void* dst,
 struct ZzCtx {
   const int32_t* cu;
   int32_t n, N;
-  const int* map;
   cudaStream_t st;
+  const int* map;  // layout position -> original token
+  const int* inv;  // original token -> layout position
 };
-ra_status zz_map(ZzCtx& z, void* map, long long total) {
-  z.map = static_cast<const int*>(map);
+// map (total int32) then its inverse (the next 256-aligned total int32) at w
+ra_status zz_map(ZzCtx& z, char* w, long long total) {
+  z.map = reinterpret_cast<const int*>(w);
+  z.inv = reinterpret_cast<const int*>(w + zz_map_bytes(total));
   TimedLaunch tl(RA_KERNEL_PERMUTE, z.st);
-  return cuda_status(launch_zigzag_varlen_map(z.cu, z.n, z.N, (int)total, static_cast<int*>(map), z.st));
+  return cuda_status(launch_zigzag_varlen_map(z.cu, z.n, z.N, (int)total, reinterpret_cast<int*>(w),
+                                              reinterpret_cast<int*>(w + zz_map_bytes(total)), z.st));
 }
 ra_status zz_in(const ZzCtx& z, const Bhsd& x, void* dst) {
   return zz_permute(x.data, x.sh, x.ss, dst, x.s * x.d, x.d, x.h, x.s, x.d, 1, z.cu, z.n, z.N, z.map, z.st);
-}
-ra_status zz_out(const ZzCtx& z, const void* src, const Bhsd& x) {
-  return zz_permute(src, x.s * x.d, x.d, x.data, x.sh, x.ss, x.h, x.s, x.d, 0, z.cu, z.n, z.N, z.map, z.st);
 }
 
 }  // namespace
@@ -694,17 +701,14 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
     char* w = static_cast<char*>(workspace);
     const size_t T = zz_tensor_bytes(total, vq.h, vq.d);
     const Bhsd q2 = zz_view(w, total, vq.h, vq.d), k2 = zz_view(w + T, total, vq.h, vq.d),
-               v2 = zz_view(w + 2 * T, total, vq.h, vq.d), o2 = zz_view(w + 3 * T, total, vq.h, vq.d);
-    float* l2 = reinterpret_cast<float*>(w + 4 * T);
-    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, nullptr, st};
-    RA_TRY(zz_map(z, w + 4 * T + zz_lse_bytes(total, vq.h), total));
+               v2 = zz_view(w + 2 * T, total, vq.h, vq.d);
+    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, st, nullptr, nullptr};
+    RA_TRY(zz_map(z, w + 3 * T, total));
     RA_TRY(zz_in(z, vq, q2.data));
     RA_TRY(zz_in(z, vk, k2.data));
     RA_TRY(zz_in(z, vv, v2.data));
-    RA_TRY(fwd_common(q2, k2, v2, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, o2, 0, l2, 0, total, 1,
-                      cu_seqlens_dev, n_seqs, stream));
-    RA_TRY(zz_out(z, o2.data, vo));
-    return zz_permute(l2, total, 1, lse->data, lsh, lss, vq.h, total, 0, 0, z.cu, z.n, z.N, z.map, st);
+    return fwd_common(q2, k2, v2, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale, -1, vo, 0,
+                      static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream, -1, z.inv);
   }
   return fwd_common(vq, vk, vv, layout, n_shards, causal, softmax_scale, -1, vo, 0,
                     static_cast<float*>(lse->data), lsb, lsh, lss, cu_seqlens_dev, n_seqs, stream);
@@ -738,23 +742,18 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
     char* w = static_cast<char*>(workspace) + SB;
     const long long h = vq.h, d = vq.d;
     const Bhsd do2 = zz_view(w, total, h, d), q2 = zz_view(w + T, total, h, d), k2 = zz_view(w + 2 * T, total, h, d),
-               v2 = zz_view(w + 3 * T, total, h, d), o2 = zz_view(w + 4 * T, total, h, d),
-               dk2 = zz_view(w + 5 * T, total, h, d), dv2 = zz_view(w + 6 * T, total, h, d);
-    float* l2 = reinterpret_cast<float*>(w + 7 * T);
-    const Bhsd& dq2 = o2;  // out is read only by the preprocess, which runs before the dQ kernel writes
-    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, nullptr, st};
-    RA_TRY(zz_map(z, w + 7 * T + zz_lse_bytes(total, h), total));
+               v2 = zz_view(w + 3 * T, total, h, d), o2 = zz_view(w + 4 * T, total, h, d);
+    float* l2 = reinterpret_cast<float*>(w + 5 * T);
+    ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, st, nullptr, nullptr};
+    RA_TRY(zz_map(z, w + 5 * T + zz_lse_bytes(total, h), total));
     RA_TRY(zz_in(z, vdo, do2.data));
     RA_TRY(zz_in(z, vq, q2.data));
     RA_TRY(zz_in(z, vk, k2.data));
     RA_TRY(zz_in(z, vv, v2.data));
     RA_TRY(zz_in(z, vo, o2.data));
     RA_TRY(zz_permute(lse->data, lsh, lss, l2, total, 1, h, total, 0, 1, z.cu, z.n, z.N, z.map, st));
-    RA_TRY(bwd_common(do2, q2, k2, v2, o2, l2, 0, total, 1, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale,
-                      dq2, dk2, dv2, workspace, SB, cu_seqlens_dev, n_seqs, stream));
-    RA_TRY(zz_out(z, dq2.data, vdq));
-    RA_TRY(zz_out(z, dk2.data, vdk));
-    return zz_out(z, dv2.data, vdv);
+    return bwd_common(do2, q2, k2, v2, o2, l2, 0, total, 1, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale,
+                      vdq, vdk, vdv, workspace, SB, cu_seqlens_dev, n_seqs, stream, -1, z.inv);
   }
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,

@@ -385,24 +385,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     });
     // ---------------- epilogue: warpgroup 1 writes the dV rows, warpgroup 2 the dK rows
     const long long prow = (long long)k.s * p.L + j;
-    __nv_bfloat16* dst = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
-                                         (long long)h * p.v_sh + prow * p.v_ss
-                                   : reinterpret_cast<__nv_bfloat16*>(p.dk) + (long long)b * p.k_sb +
-                                         (long long)h * p.k_sh + prow * p.k_ss;
+    const int* rmap = VL ? p.row_map : nullptr;  // varlen in original order: rows of the caller's layout
+    __nv_bfloat16* base = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
+                                          (long long)h * p.v_sh
+                                    : reinterpret_cast<__nv_bfloat16*>(p.dk) + (long long)b * p.k_sb +
+                                          (long long)h * p.k_sh;
+    const long long pitch = half == 0 ? p.v_ss : p.k_ss;
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(E_KV_DONE), 0, abort_flag, p.ctl, 38)) {
         tc_fence_after();
         // every MMA is done: the operand buffers hold the warps' row slots
         fence_proxy_async_smem();
         const int j_w = j - lane;  // the warp's first key row
-        const long long pitch = half == 0 ? p.v_ss : p.k_ss;
         const int nvalid = min(max(p.L - j_w, 0), 32);
         const long long row_w = (long long)k.s * p.L + j_w;  // the warp's first row of dk / dv
         if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.S), p.ctl, 14))
           store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
-                                  sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch, nvalid);
+                                  sp + (warp - 4) * (32 * D * 2), base, pitch, row_w, nvalid, rmap);
       }
     } else if (valid_k && in_bounds(prow >= 0 && prow < p.S, p.ctl, 15)) {
+      __nv_bfloat16* dst = base + (rmap ? (long long)__ldg(rmap + prow) : prow) * pitch;
       for (int u = 0; u < D / 8; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -741,8 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     });
     // ---------------- epilogue: dQ = scale * (dS K), half the head dim per thread
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) + (long long)b * p.q_sb + (long long)h * p.q_sh +
-                         (long long)(r * p.L + i - p.q_base) * p.q_ss + half * (D / 2);
+    const int* rmap = VL ? p.row_map : nullptr;  // varlen in original order: rows of the caller's layout
+    __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(p.dq) + (long long)b * p.q_sb + (long long)h * p.q_sh +
+                          half * (D / 2);
+    const long long qrow = (long long)r * p.L + i - p.q_base;
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(F_DQ_DONE), 0, abort_flag, p.ctl, 63)) {
         tc_fence_after();
@@ -752,10 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nvalid = min(max(p.L - i_w, 0), 32);
         const long long row_w = (long long)r * p.L + i_w - p.q_base;  // the warp's first row of dq
         if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.q_rows), p.ctl, 18))
-          store_rows_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, sp + (warp - 4) * (32 * D),
-                                  dst - lane * p.q_ss, p.q_ss, nvalid);
+          store_rows_bf16<D / 64>(tl + LY::kTmemDQ + half * (D / 2), p.scale, sp + (warp - 4) * (32 * D), base,
+                                  p.q_ss, row_w, nvalid, rmap);
       }
-    } else if (valid && in_bounds((long long)r * p.L + i - p.q_base < p.q_rows, p.ctl, 19)) {
+    } else if (valid && in_bounds(qrow < p.q_rows, p.ctl, 19)) {
+      __nv_bfloat16* dst = base + (rmap ? (long long)__ldg(rmap + qrow) : qrow) * p.q_ss;
       for (int u = 0; u < D / 16; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }

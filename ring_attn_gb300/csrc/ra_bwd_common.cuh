@@ -31,10 +31,13 @@ static __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[6
 // bytes: each lane writes its segment there (16-byte pieces, the piece index
 // XOR the row's low bits, so the lanes spread over the banks), then the warp
 // stores whole segments with consecutive lanes on consecutive pieces.  Rows
-// [0, nvalid) are written; dst0 is row 0's segment, stride the row pitch.
+// [0, nvalid) are written: row l goes to row row0 + l of base (pitch `stride`),
+// or, with a row map, to row rmap[row0 + l] (a varlen call computed in
+// original order that writes its results in the caller's layout order).
 template <int N32>
-static __device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul, uint8_t* slot, __nv_bfloat16* dst0,
-                                                long long stride, int nvalid) {
+static __device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul, uint8_t* slot, __nv_bfloat16* base,
+                                                       long long stride, long long row0, int nvalid,
+                                                       const int* rmap) {
   constexpr int kPieces = 4 * N32;                      // 16-byte pieces per segment
   constexpr int kSwz = kPieces < 8 ? kPieces - 1 : 7;  // XOR mask on the piece index
   const int lane = threadIdx.x & 31;
@@ -61,7 +64,10 @@ static __device__ __forceinline__ void store_rows_bf16(uint32_t taddr, float mul
   for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
     const int row = r0 + lane / kPieces;
     const uint4 v = *reinterpret_cast<const uint4*>(slot + row * kPieces * 16 + ((pc ^ (row & kSwz)) << 4));
-    if (row < nvalid) *reinterpret_cast<uint4*>(dst0 + row * stride + pc * 8) = v;
+    if (row < nvalid) {
+      const long long dr = rmap ? (long long)__ldg(rmap + row0 + row) : row0 + row;
+      *reinterpret_cast<uint4*>(base + dr * stride + pc * 8) = v;
+    }
   }
 }
 

@@ -426,24 +426,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     });
     // ---------------- epilogue: warpgroup 1 writes the dV rows, warpgroup 2 the dK rows
     const long long prow = (long long)s * p.L + j;
-    __nv_bfloat16* dst = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
-                                         (long long)h * p.v_sh + prow * p.v_ss
-                                   : reinterpret_cast<__nv_bfloat16*>(p.dk) + (long long)b * p.k_sb +
-                                         (long long)h * p.k_sh + prow * p.k_ss;
+    const int* rmap = VL ? p.row_map : nullptr;  // varlen in original order: rows of the caller's layout
+    __nv_bfloat16* base = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
+                                          (long long)h * p.v_sh
+                                    : reinterpret_cast<__nv_bfloat16*>(p.dk) + (long long)b * p.k_sb +
+                                          (long long)h * p.k_sh;
+    const long long pitch = half == 0 ? p.v_ss : p.k_ss;
     if (n_tiles > 0) {
       if (ok && wait_warp_pair(BAR(P_KV_DONE), 0, abort_flag, peer_abort, p.ctl, 96)) {
         tc_fence_after();
         // every MMA of the pair is done: this CTA's K / V buffers hold the warps' row slots
         fence_proxy_async_smem();
         const int j_w = j - lane;  // the warp's first key row
-        const long long pitch = half == 0 ? p.v_ss : p.k_ss;
         const int nvalid = min(max(p.L - j_w, 0), 32);
         const long long row_w = (long long)s * p.L + j_w;  // the warp's first row of dk / dv
         if (in_bounds(nvalid == 0 || (row_w >= 0 && row_w + nvalid <= p.S), p.ctl, 23))
           store_rows_bf16<D / 32>(tl + (half == 0 ? LY::kTmemDV : LY::kTmemDK), half == 0 ? 1.f : p.scale,
-                                  sp + (warp - 4) * (32 * D * 2), dst - lane * pitch, pitch, nvalid);
+                                  sp + (warp - 4) * (32 * D * 2), base, pitch, row_w, nvalid, rmap);
       }
     } else if (valid_k && in_bounds(prow >= 0 && prow < p.S, p.ctl, 24)) {
+      __nv_bfloat16* dst = base + (rmap ? (long long)__ldg(rmap + prow) : prow) * pitch;
       for (int u = 0; u < D / 8; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
     }
   }

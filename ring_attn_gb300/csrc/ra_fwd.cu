@@ -402,8 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     });
 
     const long long qpos = (long long)(r * p.L + i - p.q_base);  // row of q / out / lse
-    float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + qpos * p.l_ss;
     if (valid && !in_bounds(qpos >= 0 && qpos < p.q_rows, p.ctl, 3)) valid = false;  // skip this row's stores
+    // varlen computed in original order: out / lse rows of the caller's layout order
+    const int* rmap = VL ? p.row_map : nullptr;
+    const long long opos = rmap && valid ? (long long)__ldg(rmap + qpos) : qpos;
+    float* lse_ptr = p.lse + (long long)b * p.l_sb + (long long)h * p.l_sh + opos * p.l_ss;
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(B_O_DONE), 0, abort_flag, p.ctl, 9)) {
         tc_fence_after();
@@ -480,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 val = *reinterpret_cast<const uint4*>(slot + R * nch * 16 + ((pc ^ (R & 7)) << 4));
             const long long q_row = (long long)(r * p.L + i_w + R - p.q_base);
             if (i_w + R < p.L && in_bounds(q_row >= 0 && q_row < p.q_rows, p.ctl, 4)) {
-              const long long e = (long long)b * p.o_sb + (long long)h * p.o_sh + q_row * p.o_ss;
+              const long long o_row = rmap ? (long long)__ldg(rmap + q_row) : q_row;
+              const long long e = (long long)b * p.o_sb + (long long)h * p.o_sh + o_row * p.o_ss;
               *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) + e * esz + pc * 16) = val;
             }
           }
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (valid) {
       // no key tile at all (a single ring step can be empty): out = 0, lse = -inf
-      const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + qpos * p.o_ss;
+      const long long orow = (long long)b * p.o_sb + (long long)h * p.o_sh + opos * p.o_ss;
       if (p.out_f32) {
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow);
         for (int k = 0; k < D / 4; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -28,6 +28,7 @@ struct FwdParams {
   int q_base;               // token row of q / out / lse row 0 (one rank's slice: r_only * L, else 0)
   int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
   int q_rows;               // rows of q / out / lse: S, or L for one llama3 rank (bounds checks)
+  const int* row_map;       // varlen: row of out / lse for each (original-order) row, or nullptr (the same row)
   DevCtl ctl;
 };
 
@@ -52,6 +53,7 @@ struct BwdParams {
   int r_only;               // -1: every Q shard; else only this one (a llama3 rank)
   int stat_N, stat_r0;      // the statistics hold shards [stat_r0, stat_r0 + stat_N)
   int q_rows;               // rows of q / dO / out / dq: S, or L for one llama3 rank (bounds checks)
+  const int* row_map;       // varlen: row of dq / dk / dv for each (original-order) row, or nullptr (the same row)
   DevCtl ctl;
 };
 
@@ -136,7 +138,9 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 
 // map[p] = original token at layout position p of the zigzag varlen split of
 // one packed buffer of `total` tokens (N shards, cu_seqlens with n_seqs entries + 1).
-cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, cudaStream_t st);
+// With inv non-null also inv[map[p]] = p (the layout position of each original token).
+cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, int* inv,
+                                     cudaStream_t st);
 
 int num_sms();
 

@@ -250,16 +250,21 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_pre_kernel(View4 dout, View4 
 // One thread per layout position: the search of cu_seqlens that the permute
 // kernel would repeat for every row of every tensor is done once per call.
 __global__ void __launch_bounds__(kThreads) zigzag_varlen_map_kernel(const int* cu, int n_seqs, int N, int L, int total,
-                                                                     int* map) {
-  for (int p = blockIdx.x * kThreads + threadIdx.x; p < total; p += gridDim.x * kThreads)
-    map[p] = vz_token(cu, n_seqs, N, p / L, p % L);
+                                                                     int* map, int* inv) {
+  for (int p = blockIdx.x * kThreads + threadIdx.x; p < total; p += gridDim.x * kThreads) {
+    const int g = vz_token(cu, n_seqs, N, p / L, p % L);
+    map[p] = g;
+    if (inv) inv[g] = p;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, cudaStream_t st) {
+cudaError_t launch_zigzag_varlen_map(const int* cu, int n_seqs, int N, int total, int* map, int* inv,
+                                     cudaStream_t st) {
   if (N < 1 || total < 1 || total % N) return cudaErrorInvalidValue;
-  zigzag_varlen_map_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(cu, n_seqs, N, total / N, total, map);
+  zigzag_varlen_map_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(cu, n_seqs, N, total / N, total, map,
+                                                                           inv);
   return cudaGetLastError();
 }
 
