@@ -348,8 +348,6 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-legs", action="store_true", help="skip the contiguous-16k and stripe-128k legs")
-    ap.add_argument("--persistent", type=int, choices=[0, 1], default=None,
-                    help="persistent dQ kernel on (1) or off (0) (default: the library's)")
     ap.add_argument("--dkdv", choices=["pair", "one"], default=None,
                     help="dK / dV kernel at head_dim 128: CTA pairs or one CTA per key tile (default: the library's)")
     ap.add_argument("--seq", type=int, default=None, help="smaller sequence length (profiling cases only)")
@@ -387,8 +385,6 @@ def main():
     ra.load()
     if args.dkdv:
         ra.ring_attn_set_knob(ra.RA_KNOB_DKDV_PAIR, 1 if args.dkdv == "pair" else 0)
-    if args.persistent is not None:
-        ra.ring_attn_set_knob(ra.RA_KNOB_PERSISTENT, args.persistent)
     dev = torch.device("cuda", local)
     peaks = _peaks()
     if args.varlen:

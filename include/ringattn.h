@@ -294,17 +294,8 @@ ra_status ring_attn_check_device_error(void* stream, int32_t* info);
  * backward's dK / dV pass at head_dim 128 on CTA pairs (two SMs share each
  * M = 256 tensor-core MMA, halving each SM's operand reads from shared memory);
  * 0 (default) runs the one-CTA kernel, which head_dim 64 always uses.  Both
- * give the same results up to fp32 summation order.  RA_KNOB_PERSISTENT: 1
- * (default) runs the backward's dQ pass as a persistent kernel, whose CTAs take
- * over the query tiles of CTAs that have not started yet (cluster launch
- * control), so that a tile's set-up overlaps the previous one; 0 runs one
- * query tile per CTA.  The same results, bit for bit. */
-typedef enum {
-  RA_KNOB_WAIT_LIMIT_NS = 0,
-  RA_KNOB_DEBUG_FLAGS = 1,
-  RA_KNOB_DKDV_PAIR = 2,
-  RA_KNOB_PERSISTENT = 3
-} ra_knob;
+ * give the same results up to fp32 summation order. */
+typedef enum { RA_KNOB_WAIT_LIMIT_NS = 0, RA_KNOB_DEBUG_FLAGS = 1, RA_KNOB_DKDV_PAIR = 2 } ra_knob;
 ra_status ring_attn_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing (process-wide, off by default; one device per process).

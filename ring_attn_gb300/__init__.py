@@ -28,7 +28,7 @@ __all__ = [
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "stripe": 2}
 RA_BF16, RA_FP32 = 0, 1
 RA_OP_FWD, RA_OP_BWD = 0, 1
-RA_KNOB_WAIT_LIMIT_NS, RA_KNOB_DEBUG_FLAGS, RA_KNOB_DKDV_PAIR, RA_KNOB_PERSISTENT = 0, 1, 2, 3
+RA_KNOB_WAIT_LIMIT_NS, RA_KNOB_DEBUG_FLAGS, RA_KNOB_DKDV_PAIR = 0, 1, 2
 
 # Every extern "C" symbol include/ringattn.h declares.
 EXPORTED_SYMBOLS = (

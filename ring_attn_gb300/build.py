@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
 BUILD_DBG = os.path.join(PKG, "_build_dbg")
 LIB_DBG = os.path.join(PKG, "libringattn_dbg.so")
-SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_dkdv_pair.cu", "ra_dq_persist.cu", "ra_simple.cu"]
+SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_dkdv_pair.cu", "ra_simple.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ra_device.cuh", "ra_internal.h", "ra_tiles.cuh", "ra_bwd_common.cuh")] + [
     os.path.join(ROOT, "include", "ringattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

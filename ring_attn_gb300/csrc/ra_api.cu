@@ -21,7 +21,6 @@ std::mutex g_mu;
 unsigned long long g_wait_limit_ns = 4000000000ull;
 int g_debug_flags = 0;
 int g_dkdv_pair = 0;  // head_dim 128: 1 runs the dK / dV pass on CTA pairs
-int g_persistent = 1;  // 1: persistent kernels (cluster launch control) where built
 int* g_err_ptr[64] = {nullptr};
 
 ra_status dev_ctl(DevCtl* c) {
@@ -361,8 +360,6 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
     RA_TRY(cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 0, st)));
   }
   TimedLaunch tl(RA_KERNEL_BWD_DQ, st);
-  if (__atomic_load_n(&g_persistent, __ATOMIC_RELAXED))
-    return cuda_status(launch_dq_persist((int)q.d, tq, tk, tv, tdo, p, st));
   return cuda_status(launch_bwd((int)q.d, tq, tk, tv, tdo, p, 1, st));
 }
 
@@ -964,11 +961,6 @@ ra_status ring_attn_set_knob(int32_t knob, int64_t value) {
   if (knob == RA_KNOB_DKDV_PAIR) {
     if (value < 0 || value > 1) return RA_ERR_INVALID_ARG;
     __atomic_store_n(&g_dkdv_pair, (int)value, __ATOMIC_RELAXED);
-    return RA_OK;
-  }
-  if (knob == RA_KNOB_PERSISTENT) {
-    if (value < 0 || value > 1) return RA_ERR_INVALID_ARG;
-    __atomic_store_n(&g_persistent, (int)value, __ATOMIC_RELAXED);
     return RA_OK;
   }
   return RA_ERR_INVALID_ARG;

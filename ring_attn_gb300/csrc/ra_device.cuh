@@ -324,38 +324,6 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
-// ------------------------------------------------------------------ cluster launch control
-// A running CTA asks the hardware to cancel the launch of a CTA that has not
-// started yet and takes over its work (its blockIdx): a persistent kernel keeps
-// the hardware's own order and load balance, and a CTA's set-up and its next
-// work item's loads overlap its current item.  The 16-byte response lands in
-// shared memory; completion is signalled on `bar` as 16 transaction bytes.
-// After a response that reports failure no further request may be made.
-__device__ __forceinline__ void clc_try_cancel(uint32_t resp_smem, uint32_t bar) {
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-          resp_smem),
-      "r"(bar)
-      : "memory");
-}
-// Decodes a response: true and the first blockIdx of the cancelled launch, or false.
-__device__ __forceinline__ bool clc_query(uint32_t resp_smem, int& bx, int& by) {
-  uint32_t ok, x, y;
-  asm volatile(
-      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
-      "ld.shared.b128 r, [%3];\n\t"
-      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t"
-      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
-      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::y.b32.b128 %2, r;\n\t}\n"
-      : "=r"(ok), "=r"(x), "=r"(y)
-      : "r"(resp_smem)
-      : "memory");
-  bx = (int)x;
-  by = (int)y;
-  return ok != 0;
-}
-
 // Instruction descriptor for kind::f16: bf16 A and B, fp32 D, dense.
 // a_mn / b_mn: 0 = K-major, 1 = MN-major operand in shared memory.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {

@@ -83,11 +83,6 @@ size_t fwd_smem_bytes(int D);
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int which, cudaStream_t st);
 
-// The dQ kernel as a persistent kernel: a CTA takes over the query tiles of
-// CTAs that have not started (cluster launch control).
-cudaError_t launch_dq_persist(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
-
 // The dK / dV kernel on CTA pairs (cta_group::2), head_dim 128 only.  The four
 // tensor maps have 64 x 64 boxes (64 head dims by 64 rows).
 cudaError_t launch_dkdv_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -224,10 +224,6 @@ def test_knobs(lib):
     assert lib.ring_attn_set_knob(2, 5) == 1
     assert lib.ring_attn_set_knob(2, 0) == 0
     assert lib.ring_attn_set_knob(2, 1) == 0
-    assert lib.ring_attn_set_knob(2, 0) == 0
-    assert lib.ring_attn_set_knob(3, 2) == 1
-    assert lib.ring_attn_set_knob(3, 0) == 0
-    assert lib.ring_attn_set_knob(3, 1) == 0
     assert lib.ring_attn_set_knob(0, 4_000_000_000) == 0
     assert lib.ring_attn_set_knob(1, 0) == 0
 
