@@ -99,14 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y / p.H, h = blockIdx.y % p.H;
 
-  KRange k;
-  make_krange(p, (int)blockIdx.x / p.n_ktiles, ((int)blockIdx.x % p.n_ktiles) * kTileN, k);
-  int n_tiles = 0;
-  walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
-    ++n_tiles;
-    return true;
-  });
-
+  const int ks = (int)blockIdx.x / p.n_ktiles, kj0 = ((int)blockIdx.x % p.n_ktiles) * kTileN;
   const uint32_t bar0 = sb + LY::kBar;
   auto BAR = [bar0](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + LY::kMisc + 4);
@@ -127,16 +120,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(E_TEARDOWN), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    // the key tile's K and V depend on nothing the walk below computes: issued
+    // first, their latency overlaps the CTA's set-up
+    const int krow = ks * p.L + kj0;
+    mbar_expect_tx(BAR(E_KV_FULL), 2 * LY::kTile);
+    for (int c = 0; c < D / 64; ++c)
+      if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, krow, h, b), p.ctl, 10)) {
+        tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, h, b);
+        tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
+      }
+  }
+  KRange k;
+  make_krange(p, ks, kj0, k);
+  int n_tiles = 0;
+  walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
+    ++n_tiles;
+    return true;
+  });
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -150,13 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_tiles > 0) {
       int issued[2] = {0, 0};
-      const int krow = k.s * p.L + k.j0;
-      mbar_expect_tx(BAR(E_KV_FULL), 2 * LY::kTile);
-      for (int c = 0; c < D / 64; ++c)
-        if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, krow, h, b), p.ctl, 10)) {
-          tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, h, b);
-          tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
-        }
       int i = 0;
       walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
         const int st = i & 1;
@@ -185,13 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++i;
         return true;
       });
-      drain_one(BAR(E_KV_FULL), 0, p.ctl, 40);
       for (int st = 0; st < 2; ++st)
         if (issued[st]) {
           drain_one(BAR(E_Q_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
           drain_one(BAR(E_DO_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
         }
     }
+    if (lane == 0) drain_one(BAR(E_KV_FULL), 0, p.ctl, 40);  // issued at entry
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -486,15 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     r = p.r_only >= 0 ? p.r_only : x / p.n_qtiles;
     i0 = (x % p.n_qtiles) * kTileM;
   }
-  QRange qr;
-  make_qrange(p, r, i0, kTileM, qr);
-  const int nkt = (p.L + kTileN - 1) / kTileN;
-  int n_tiles = 0;
-  walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int, int) {
-    ++n_tiles;
-    return true;
-  });
-
   const uint32_t bar0 = sb + LY::kBar;
   auto BAR = [bar0](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + LY::kMisc + 4);
@@ -518,16 +509,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(F_TEARDOWN), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    // the tile's Q and dO depend on nothing the tile walk below computes:
+    // issued first, their latency overlaps the CTA's set-up
+    const int qrow = r * p.L + i0 - p.q_base;
+    mbar_expect_tx(BAR(F_QDO_FULL), 2 * LY::kTile);
+    for (int c = 0; c < D / 64; ++c)
+      if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 16)) {
+        tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
+        tma_load_4d(sb + LY::kDO + c * kBox, &tmDO, BAR(F_QDO_FULL), c * 64, qrow, h, b);
+      }
+  }
+  QRange qr;
+  make_qrange(p, r, i0, kTileM, qr);
+  const int nkt = (p.L + kTileN - 1) / kTileN;
+  int n_tiles = 0;
+  walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int, int) {
+    ++n_tiles;
+    return true;
+  });
+
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -538,22 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producers
     if (lane == 0 && n_tiles > 0) {
       const bool is_k = warp == 0;
-      bool q_issued = false;
       int issued[3] = {0, 0, 0};
       const int nst = is_k ? KS : VS;
       const int full0 = is_k ? F_K_FULL : F_V_FULL, empty0 = is_k ? F_K_EMPTY : F_V_EMPTY;
       const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
       const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
-      if (is_k) {
-        const int qrow = r * p.L + i0 - p.q_base;
-        mbar_expect_tx(BAR(F_QDO_FULL), 2 * LY::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 16)) {
-            tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
-            tma_load_4d(sb + LY::kDO + c * kBox, &tmDO, BAR(F_QDO_FULL), c * 64, qrow, h, b);
-          }
-        q_issued = true;
-      }
       int j = 0;
       walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int s, int kt) {
         const int st = j % nst;
@@ -567,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++j;
         return true;
       });
-      if (q_issued) drain_one(BAR(F_QDO_FULL), 0, p.ctl, 53);
       for (int st = 0; st < nst; ++st)
         if (issued[st]) drain_one(BAR(full0 + st), (issued[st] - 1) & 1, p.ctl, 54);
     }
+    if (threadIdx.x == 0) drain_one(BAR(F_QDO_FULL), 0, p.ctl, 53);  // issued at entry
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -120,20 +120,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     r = p.r_only >= 0 ? p.r_only : x / n_pairs;
     i0 = (x % n_pairs) * kRowsPerCta;
   }
-  QRange cta;  // both query tiles together: decides which key tiles are visited
-  make_qrange(p, r, i0, kRowsPerCta, cta);
-  const int nkt = (p.L + kTileN - 1) / kTileN;
-  int n_tiles = 0;
-  walk_tiles(p, cta, nkt, [&](int, int) {
-    ++n_tiles;
-    return true;
-  });
-
   const uint32_t bar0 = sb + LY::kBar;
   auto BAR = [bar0](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + LY::kMisc + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sp + LY::kMisc);
 
+  bool q_issued = false;  // by thread 0, the Q / K producer
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q_FULL), 1);
     for (int i = 0; i < kKStages; ++i) {
@@ -152,15 +144,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_TEARDOWN), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    // the CTA's Q tiles depend on nothing the tile walk below computes: issued
+    // first, their latency overlaps the CTA's set-up
+    if (!(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
+      const int prow0 = r * p.L + i0 - p.q_base;
+      mbar_expect_tx(BAR(B_Q_FULL), kQTiles * LY::kTile);
+      for (int t = 0; t < kQTiles; ++t)
+        for (int c = 0; c < D / 64; ++c)
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, prow0 + t * kTileM, h, b), p.ctl, 1))
+            tma_load_4d(sb + LY::kQ + t * LY::kTile + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0 + t * kTileM, h,
+                        b);
+      q_issued = true;
+    }
+  }
+  QRange cta;  // both query tiles together: decides which key tiles are visited
+  make_qrange(p, r, i0, kRowsPerCta, cta);
+  const int nkt = (p.L + kTileN - 1) / kTileN;
+  int n_tiles = 0;
+  walk_tiles(p, cta, nkt, [&](int, int) {
+    ++n_tiles;
+    return true;
+  });
+
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -175,22 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the V ring, which frees a stage only once both PV MMAs of a tile are done
     if (lane == 0 && n_tiles > 0) {
       const bool is_k = warp == 0;
-      bool q_issued = false;
       int issued[kKStages] = {};
       const int nst = is_k ? kKStages : kVStages;
       const int full0 = is_k ? B_K_FULL : B_V_FULL, empty0 = is_k ? B_K_EMPTY : B_V_EMPTY;
       const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
       const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
-      if (is_k && !(p.ctl.debug_flags & DBG_SKIP_Q_LOAD)) {
-        const int prow0 = r * p.L + i0 - p.q_base;
-        mbar_expect_tx(BAR(B_Q_FULL), kQTiles * LY::kTile);
-        for (int t = 0; t < kQTiles; ++t)
-          for (int c = 0; c < D / 64; ++c)
-            if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, prow0 + t * kTileM, h, b), p.ctl, 1))
-              tma_load_4d(sb + LY::kQ + t * LY::kTile + c * kBox, &tmQ, BAR(B_Q_FULL), c * 64, prow0 + t * kTileM,
-                          h, b);
-        q_issued = true;
-      }
       int j = 0;
       walk_tiles(p, cta, nkt, [&](int s, int kt) {
         const int st = j % nst;
@@ -206,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       });
       // every issued copy lands before the CTA may exit
-      if (q_issued) drain_one(BAR(B_Q_FULL), 0, p.ctl, 20);
       for (int st = 0; st < nst; ++st)
         if (issued[st]) drain_one(BAR(full0 + st), (issued[st] - 1) & 1, p.ctl, 21);
     }
+    if (threadIdx.x == 0 && q_issued) drain_one(BAR(B_Q_FULL), 0, p.ctl, 20);
     __syncwarp();
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
