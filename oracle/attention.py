@@ -184,14 +184,26 @@ def block_attention(q, k, v, gq, gk, scale, causal, segq=None, segk=None):
     return out, lse
 
 
+def _kv_head(hi, h, hk):
+    """Key / value head of query head hi when h query heads share hk key / value
+    heads (grouped-query attention): consecutive groups of h / hk query heads
+    share one, as in flash-attention's "non-equal head counts"; hk == h is plain
+    multi-head attention."""
+    if h % hk:
+        raise ValueError(f"{h} query heads do not split into groups over {hk} key/value heads")
+    return hi // (h // hk)
+
+
 def attention_fwd(q, k, v, scale, causal, cu_seqlens=None, row_block=1024):
     """Full softmax attention in original token order.
 
-    q, k, v: (b, h, s, d) (any float type; upcast exactly to fp64).
-    Returns out (b, h, s, d) and lse (b, h, s), fp64.
+    q: (b, h, s, d); k, v: (b, hk, s, d) with h a multiple of hk (query head hi
+    attends with key / value head hi // (h / hk)); any float type, upcast
+    exactly to fp64.  Returns out (b, h, s, d) and lse (b, h, s), fp64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     b, h, s, d = q.shape
+    hk = k.shape[1]
     t = np.arange(s)
     seg = segment_ids(cu_seqlens, s) if cu_seqlens is not None else None
     out = np.empty_like(q)
@@ -201,7 +213,8 @@ def attention_fwd(q, k, v, scale, causal, cu_seqlens=None, row_block=1024):
             for r0 in range(0, s, row_block):
                 r1 = min(s, r0 + row_block)
                 kend = r1 if causal else s  # keys past the block's last row are masked anyway
-                o, l = block_attention(q[bi, hi, r0:r1], k[bi, hi, :kend], v[bi, hi, :kend],
+                kh = _kv_head(hi, h, hk)
+                o, l = block_attention(q[bi, hi, r0:r1], k[bi, kh, :kend], v[bi, kh, :kend],
                                        t[r0:r1], t[:kend], scale, causal,
                                        None if seg is None else seg[r0:r1],
                                        None if seg is None else seg[:kend])
@@ -215,10 +228,13 @@ def attention_bwd(q, k, v, do, scale, causal, cu_seqlens=None, row_block=1024):
 
       P = exp(S - lse), D_i = sum_d dO_id out_id
       dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q
-    Returns dq, dk, dv (b, h, s, d) fp64.
+    With fewer key / value heads than query heads (grouped-query attention) the
+    gradient of a shared key / value head is the sum over its query heads.
+    Returns dq (b, h, s, d) and dk, dv (b, hk, s, d), fp64.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     b, h, s, d = q.shape
+    hk = k.shape[1]
     out, lse = attention_fwd(q, k, v, scale, causal, cu_seqlens, row_block)
     t = np.arange(s)
     seg = segment_ids(cu_seqlens, s) if cu_seqlens is not None else None
@@ -228,18 +244,19 @@ def attention_bwd(q, k, v, do, scale, causal, cu_seqlens=None, row_block=1024):
     D = (do * out).sum(axis=-1)
     for bi in range(b):
         for hi in range(h):
+            kh = _kv_head(hi, h, hk)
             for r0 in range(0, s, row_block):
                 r1 = min(s, r0 + row_block)
-                S = scale * (q[bi, hi, r0:r1] @ k[bi, hi].T)
+                S = scale * (q[bi, hi, r0:r1] @ k[bi, kh].T)
                 mask = _allowed(t[r0:r1], t, causal,
                                 None if seg is None else seg[r0:r1],
                                 None if seg is None else seg)
                 P = np.where(mask, np.exp(S - lse[bi, hi, r0:r1, None]), 0.0)
-                dv[bi, hi] += P.T @ do[bi, hi, r0:r1]
-                dP = do[bi, hi, r0:r1] @ v[bi, hi].T
+                dv[bi, kh] += P.T @ do[bi, hi, r0:r1]
+                dP = do[bi, hi, r0:r1] @ v[bi, kh].T
                 dS = P * (dP - D[bi, hi, r0:r1, None])
-                dq[bi, hi, r0:r1] = scale * (dS @ k[bi, hi])
-                dk[bi, hi] += scale * (dS.T @ q[bi, hi, r0:r1])
+                dq[bi, hi, r0:r1] = scale * (dS @ k[bi, kh])
+                dk[bi, kh] += scale * (dS.T @ q[bi, hi, r0:r1])
     return dq, dk, dv
 
 

@@ -544,3 +544,71 @@ def test_planted_gradient_sign_error_fails_a_pin(monkeypatch):
     monkeypatch.setattr(A, "attention_bwd", mutant)
     monkeypatch.setattr(oracle, "attention_bwd", mutant)
     assert not _pins_hold()
+
+
+# --------------------------------------------------------------------------- grouped-query attention
+def _gqa_inputs(h, hk, s, d, seed):
+    x = _inputs(1, h, s, d, seed, with_do=True)
+    return {"q": x["q"], "k": x["k"][:, :hk], "v": x["v"][:, :hk], "do": x["do"]}
+
+
+@pytest.mark.parametrize("h,hk", [(4, 1), (4, 2), (6, 3), (3, 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_matches_torch_sdpa_enable_gqa(h, hk, causal):
+    """Grouped-query heads against torch's own grouped-query attention (float64,
+    autograd): query head i uses key / value head i // (h / hk)."""
+    x = _gqa_inputs(h, hk, 20, 8, 300 + h + hk)
+    sc = 0.4
+    tq, tk, tv = (torch.tensor(x[n], dtype=torch.float64, requires_grad=True) for n in ("q", "k", "v"))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=sc, enable_gqa=True)
+    out.backward(torch.tensor(x["do"], dtype=torch.float64))
+    o, _ = oracle.attention_fwd(x["q"], x["k"], x["v"], sc, causal)
+    dq, dk, dv = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], sc, causal)
+    np.testing.assert_allclose(o, out.detach().numpy(), rtol=0, atol=1e-12)
+    for a, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert a.shape == ref.shape
+        np.testing.assert_allclose(a, ref.numpy(), rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_gradient_central_finite_differences(causal):
+    """The gradient of a shared key / value head collects every query head of its group."""
+    s, d, h, hk = 10, 4, 4, 2
+    x = _gqa_inputs(h, hk, s, d, 33)
+    cu = cu_seqlens([4, 6])
+    sc = 0.5
+    dq, dk, dv = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], sc, causal, cu_seqlens=cu)
+
+    def loss(q, k, v):
+        out, _ = oracle.attention_fwd(q, k, v, sc, causal, cu_seqlens=cu)
+        return float((x["do"] * out).sum())
+
+    eps = 1e-6
+    for name, grad in (("q", dq), ("k", dk), ("v", dv)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            args = {n: x[n].copy() for n in ("q", "k", "v")}
+            args[name][idx] += eps
+            fp = loss(args["q"], args["k"], args["v"])
+            args[name][idx] -= 2 * eps
+            fm = loss(args["q"], args["k"], args["v"])
+            num[idx] = (fp - fm) / (2 * eps)
+        rel = np.linalg.norm(num - grad) / max(np.linalg.norm(grad), 1e-30)
+        assert rel <= 1e-6, (name, rel)
+
+
+def test_gqa_planted_interleaved_grouping_is_caught(monkeypatch):
+    """A plausible mistake, key / value head i % hk instead of i // (h / hk),
+    fails the torch comparison."""
+    x = _gqa_inputs(4, 2, 12, 8, 41)
+    tq, tk, tv = (torch.tensor(x[n], dtype=torch.float64) for n in ("q", "k", "v"))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=0.5, enable_gqa=True)
+    monkeypatch.setattr(A, "_kv_head", lambda hi, h, hk: hi % hk)
+    o, _ = oracle.attention_fwd(x["q"], x["k"], x["v"], 0.5, True)
+    assert np.abs(o - ref.numpy()).max() > 1e-3
+
+
+def test_gqa_rejects_head_counts_that_do_not_group():
+    x = _gqa_inputs(4, 3, 8, 4, 42)
+    with pytest.raises(ValueError):
+        oracle.attention_fwd(x["q"], x["k"], x["v"], 0.5, True)
