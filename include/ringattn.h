@@ -39,9 +39,13 @@
  *     wait that ran out) are reported by ring_attn_check_device_error.  On
  *     any error the outputs are unspecified.
  *   - Layout constraints for attention calls: head_dim d in {64, 128}; q, k,
- *     v (and out, dout, dq, dk, dv) have the same shape; every stride but the
- *     last is a multiple of 8 elements and every base pointer is 16-byte
- *     aligned (TMA tiles), else RA_ERR_ALIGNMENT.
+ *     v (and out, dout, dq, dk, dv) have the same shape, except that k and v
+ *     (and dk, dv) may have hk heads where hk divides q's h (grouped-query
+ *     attention: query head i attends with key / value head i / (h / hk),
+ *     integer division; the pages only use hk = h, and every call below that
+ *     says "(b, h, s, d)" for k or v accepts hk in place of h); every stride
+ *     but the last is a multiple of 8 elements and every base pointer is
+ *     16-byte aligned (TMA tiles), else RA_ERR_ALIGNMENT.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
@@ -129,9 +133,12 @@ ra_status lse_merge(ra_tensor* out_acc, ra_tensor* lse_acc, const ra_tensor* out
  *   dK = scale dS^T Q.  One kernel per key tile keeps dK and dV in tensor
  *   memory while it meets the query tiles in ring order; one kernel per query
  *   tile recomputes S and dP and keeps dQ in tensor memory.  No atomics: the
- *   results are deterministic.
+ *   results are deterministic.  With grouped key / value heads (hk < h), dK
+ *   and dV of a key / value head sum over its h / hk query heads, all met by
+ *   the same key-tile kernel in head order.
  *   workspace: at least ring_attn_workspace_size(RA_OP_BWD, b, h, s, d, n_shards)
- *   bytes, 256-byte aligned, owned by the caller, need not be initialised. */
+ *   bytes (h: q's head count), 256-byte aligned, owned by the caller, need not
+ *   be initialised. */
 ra_status ring_attn_bwd(const ra_tensor* dout, const ra_tensor* q, const ra_tensor* k, const ra_tensor* v,
                         const ra_tensor* out, const ra_tensor* lse, int32_t layout, int32_t n_shards,
                         int32_t causal, float softmax_scale, ra_tensor* dq, ra_tensor* dk, ra_tensor* dv,

@@ -124,6 +124,13 @@ ra_status check_thd(const ra_tensor* t, long long total, Bhsd* v) {
 
 bool same_shape(const Bhsd& a, const Bhsd& b) { return a.b == b.b && a.h == b.h && a.s == b.s && a.d == b.d; }
 
+// k / v against q: the same batch and head dim, and (grouped-query attention)
+// a head count that divides q's; s_ratio = k rows per q row (1, or N for one
+// llama3 rank holding L = S / N query rows).
+bool kv_matches_q(const Bhsd& q, const Bhsd& k, long long s_ratio) {
+  return q.b == k.b && q.d == k.d && k.h >= 1 && q.h % k.h == 0 && q.s * s_ratio == k.s;
+}
+
 ra_status check_layout(int32_t layout, int32_t n_shards, long long s) {
   if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_STRIPE) return RA_ERR_INVALID_ARG;
   if (n_shards < 1 || s % n_shards != 0) return RA_ERR_INVALID_ARG;
@@ -206,9 +213,8 @@ ra_status bwd_check_args(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const B
   if (!same_shape(k, v) || !same_shape(k, dk) || !same_shape(k, dv) || !same_shape(q, out) ||
       !same_shape(q, dout) || !same_shape(q, dq))
     return RA_ERR_INVALID_ARG;
-  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
-  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
-    return RA_ERR_INVALID_ARG;
+  if (rank < 0 && !kv_matches_q(q, k, 1)) return RA_ERR_INVALID_ARG;
+  if (rank >= 0 && (rank >= n_shards || !kv_matches_q(q, k, n_shards))) return RA_ERR_INVALID_ARG;
   if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
   RA_TRY(check_layout(layout, n_shards, k.s));
   RA_TRY(check_scale(scale));
@@ -224,9 +230,8 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
                      long long lss, const int32_t* cu_dev, int32_t n_seqs, void* stream, int32_t rank = -1,
                      const int* row_map = nullptr) {
   if (!same_shape(k, v) || !same_shape(q, o)) return RA_ERR_INVALID_ARG;
-  if (rank < 0 && !same_shape(q, k)) return RA_ERR_INVALID_ARG;
-  if (rank >= 0 && (q.b != k.b || q.h != k.h || q.d != k.d || rank >= n_shards || q.s * n_shards != k.s))
-    return RA_ERR_INVALID_ARG;
+  if (rank < 0 && !kv_matches_q(q, k, 1)) return RA_ERR_INVALID_ARG;
+  if (rank >= 0 && (rank >= n_shards || !kv_matches_q(q, k, n_shards))) return RA_ERR_INVALID_ARG;
   if (q.d != 64 && q.d != 128) return RA_ERR_UNSUPPORTED;
   RA_TRY(check_layout(layout, n_shards, k.s));
   RA_TRY(check_scale(scale));
@@ -238,6 +243,8 @@ ra_status fwd_common(const Bhsd& q, const Bhsd& k, const Bhsd& v, int32_t layout
   memset(&p, 0, sizeof(p));
   p.B = (int)q.b;
   p.H = (int)q.h;
+  p.Hk = (int)k.h;
+  p.G = (int)(q.h / k.h);
   p.N = n_shards;
   p.S = (int)k.s;
   p.L = (int)(k.s / n_shards);
@@ -305,6 +312,8 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   memset(&p, 0, sizeof(p));
   p.B = (int)q.b;
   p.H = (int)q.h;
+  p.Hk = (int)k.h;
+  p.G = (int)(q.h / k.h);
   p.N = n_shards;
   p.S = (int)k.s;
   p.L = (int)(k.s / n_shards);
@@ -347,7 +356,7 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
     RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, p.ctl, st)));
   }
-  if (q.d == 128 && __atomic_load_n(&g_dkdv_pair, __ATOMIC_RELAXED)) {
+  if (q.d == 128 && q.h == k.h && __atomic_load_n(&g_dkdv_pair, __ATOMIC_RELAXED)) {
     CUtensorMap pq, pk, pv, pdo;  // 64-row boxes: the pair kernel loads 64 x 64 blocks
     RA_TRY(make_tmap(q, &pq, 64));
     RA_TRY(make_tmap(k, &pk, 64));
@@ -692,7 +701,7 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
   RA_TRY(check_lse(lse, 1, vq.h, total, &lsb, &lsh, &lss));
   if (layout == RA_LAYOUT_ZIGZAG && workspace && workspace_bytes >= zz_fwd_bytes(total, vq.h, vq.d)) {
     // original-order path: the same checks as the kernels' before any launch
-    if (!same_shape(vq, vk) || !same_shape(vq, vv) || !same_shape(vq, vo)) return RA_ERR_INVALID_ARG;
+    if (!kv_matches_q(vq, vk, 1) || !same_shape(vk, vv) || !same_shape(vq, vo)) return RA_ERR_INVALID_ARG;
     if (vq.d != 64 && vq.d != 128) return RA_ERR_UNSUPPORTED;
     RA_TRY(check_scale(softmax_scale));
     if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
@@ -700,8 +709,9 @@ ra_status ring_attn_varlen_fwd(const ra_tensor* q, const ra_tensor* k, const ra_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* w = static_cast<char*>(workspace);
     const size_t T = zz_tensor_bytes(total, vq.h, vq.d);
-    const Bhsd q2 = zz_view(w, total, vq.h, vq.d), k2 = zz_view(w + T, total, vq.h, vq.d),
-               v2 = zz_view(w + 2 * T, total, vq.h, vq.d);
+    // (k and v may have fewer heads than q: their copies use the first part of each T)
+    const Bhsd q2 = zz_view(w, total, vq.h, vq.d), k2 = zz_view(w + T, total, vk.h, vq.d),
+               v2 = zz_view(w + 2 * T, total, vk.h, vq.d);
     ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, st, nullptr, nullptr};
     RA_TRY(zz_map(z, w + 3 * T, total));
     RA_TRY(zz_in(z, vq, q2.data));
@@ -741,8 +751,9 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
     const size_t SB = bwd_ws_bytes(1, vq.h, total, n_shards), T = zz_tensor_bytes(total, vq.h, vq.d);
     char* w = static_cast<char*>(workspace) + SB;
     const long long h = vq.h, d = vq.d;
-    const Bhsd do2 = zz_view(w, total, h, d), q2 = zz_view(w + T, total, h, d), k2 = zz_view(w + 2 * T, total, h, d),
-               v2 = zz_view(w + 3 * T, total, h, d), o2 = zz_view(w + 4 * T, total, h, d);
+    const long long hk = vk.h;  // k and v may have fewer heads than q
+    const Bhsd do2 = zz_view(w, total, h, d), q2 = zz_view(w + T, total, h, d), k2 = zz_view(w + 2 * T, total, hk, d),
+               v2 = zz_view(w + 3 * T, total, hk, d), o2 = zz_view(w + 4 * T, total, h, d);
     float* l2 = reinterpret_cast<float*>(w + 5 * T);
     ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, st, nullptr, nullptr};
     RA_TRY(zz_map(z, w + 5 * T + zz_lse_bytes(total, h), total));

@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sp = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.y / p.H, h = blockIdx.y % p.H;
+  // one key / value head; with grouped-query attention its G query heads share it
+  const int b = blockIdx.y / p.Hk, hk = blockIdx.y % p.Hk;
 
   const int ks = (int)blockIdx.x / p.n_ktiles, kj0 = ((int)blockIdx.x % p.n_ktiles) * kTileN;
   const uint32_t bar0 = sb + LY::kBar;
@@ -129,18 +130,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int krow = ks * p.L + kj0;
     mbar_expect_tx(BAR(E_KV_FULL), 2 * LY::kTile);
     for (int c = 0; c < D / 64; ++c)
-      if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, krow, h, b), p.ctl, 10)) {
-        tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, h, b);
-        tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, h, b);
+      if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, krow, hk, b), p.ctl, 10)) {
+        tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, hk, b);
+        tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, hk, b);
       }
   }
   KRange k;
   make_krange(p, ks, kj0, k);
-  int n_tiles = 0;
+  int n_tiles = 0;  // over all query heads of the group (every head meets the same tiles)
   walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int, int) {
     ++n_tiles;
     return true;
   });
+  n_tiles *= p.G;
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -149,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const long long stat_bh = ((long long)b * p.H + h) * p.stat_N * p.stat_L;  // statistics row of (b, h, first shard)
 
   if (warp < 4) {
     regs_dec<kDkdvRegsLow>();
@@ -158,10 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       int issued[2] = {0, 0};
       int i = 0;
-      walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
+      auto load = [&](int h, int r, int qt) {
         const int st = i & 1;
         const uint32_t par = ((i >> 1) - 1) & 1;
         const int qrow = r * p.L + qt * kTileM - p.q_base;
+        const long long stat_bh = ((long long)b * p.H + h) * p.stat_N * p.stat_L;  // (b, h, first shard)
         if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) return false;
         // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
         const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
@@ -184,7 +186,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued[st];
         ++i;
         return true;
-      });
+      };
+      // (one head per key head kept apart: the producer runs on few registers)
+      if (p.G == 1)
+        walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) { return load(hk, r, qt); });
+      else
+        walk_group_q_tiles<kTileM>(p, k, p.n_qtiles, hk, load);
       for (int st = 0; st < 2; ++st)
         if (issued[st]) {
           drain_one(BAR(E_Q_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       gk = tok(p, k.s, valid_k ? j : k.j_last);
     bool ok = true;
     int i = 0;
-    walk_q_tiles<kTileM>(p, k, p.n_qtiles, [&](int r, int qt) {
+    auto tile = [&](int r, int qt) {
       const int st = i & 1;
       // padding query rows have -lse2 = -inf and -D = 0 (P = 0, dS = 0) without a mask
       int c_lo = 0, c_hi = kTileM;
@@ -382,14 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(BAR(E_PS_FULL));
       ++i;
       return true;
-    });
+    };
+    // every query head of the group meets the same tiles; the walk does not depend on the head
+    for (int g = 0; ok && g < p.G; ++g) walk_q_tiles<kTileM>(p, k, p.n_qtiles, tile);
     // ---------------- epilogue: warpgroup 1 writes the dV rows, warpgroup 2 the dK rows
     const long long prow = (long long)k.s * p.L + j;
     const int* rmap = VL ? p.row_map : nullptr;  // varlen in original order: rows of the caller's layout
     __nv_bfloat16* base = half == 0 ? reinterpret_cast<__nv_bfloat16*>(p.dv) + (long long)b * p.v_sb +
-                                          (long long)h * p.v_sh
+                                          (long long)hk * p.v_sh
                                     : reinterpret_cast<__nv_bfloat16*>(p.dk) + (long long)b * p.k_sb +
-                                          (long long)h * p.k_sh;
+                                          (long long)hk * p.k_sh;
     const long long pitch = half == 0 ? p.v_ss : p.k_ss;
     if (n_tiles > 0) {
       if (ok && wait_warp(BAR(E_KV_DONE), 0, abort_flag, p.ctl, 38)) {
@@ -474,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.y / p.H, h = blockIdx.y % p.H;
+  const int hk = h / p.G;  // the key / value head of query head h (grouped-query attention)
   // causal: the later query tiles carry more work, start them first (the
   // batched zigzag split by chunk, so that every head's heaviest tiles lead)
   int r, i0;
@@ -557,8 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         mbar_expect_tx(BAR(full0 + st), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, s * p.L + kt * kTileN, h, b), p.ctl, 17))
-            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl, 17))
+            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, hk,
+                        b);
         ++issued[st];
         ++j;
         return true;
@@ -778,7 +789,7 @@ cudaError_t launch_bwd_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     // the register split inside the kernel is only safe with the launch allocation it was sized for
     cudaError_t e = configure_kernel<ring_dkdv_kernel<D, VL>>(kDkdvLaunchRegs, DkdvLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.N * p.n_ktiles), (unsigned)(p.B * p.H));
+    dim3 grid((unsigned)(p.N * p.n_ktiles), (unsigned)(p.B * p.Hk));
     ring_dkdv_kernel<D, VL><<<grid, kThreads, DkdvLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, pv);
   } else {
     cudaError_t e = configure_kernel<ring_dq_kernel<D, VL>>(0, DqLayout<D>::kAlloc);

@@ -198,9 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= nst && !wait_one(BAR(empty0 + st), (j / nst - 1) & 1, abort_flag, p.ctl, is_k ? 1 : 10))
           return false;
         mbar_expect_tx(BAR(full0 + st), LY::kTile);
+        // the key / value head of query head h (grouped-query attention), derived
+        // here rather than held across the walk: the producers run on few registers
+        const int hk = (int)(blockIdx.y % p.H) / p.G;
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.H, p.B}, c * 64, s * p.L + kt * kTileN, h, b), p.ctl, 2))
-            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, h, b);
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl, 2))
+            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, hk, b);
         ++issued[st];
         ++j;
         return true;

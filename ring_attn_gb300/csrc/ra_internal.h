@@ -13,7 +13,8 @@ constexpr int kTileM = 128;   // query rows per tile
 constexpr int kTileN = 128;   // key rows per tile
 
 struct FwdParams {
-  int B, H, N, L, S;        // batch, heads, shards, tokens per shard, total tokens
+  int B, H, N, L, S;        // batch, query heads, shards, tokens per shard, total tokens
+  int Hk, G;                // key / value heads; query heads per key / value head (H = G * Hk)
   int layout, causal;
   int step;                 // -1: fused ring over all N steps; else one ring step
   int n_qtiles;             // ceil(L / 128)
@@ -33,7 +34,8 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  int B, H, N, L, S;
+  int B, H, N, L, S;        // batch, query heads, shards, tokens per shard, total tokens
+  int Hk, G;                // key / value heads; query heads per key / value head (H = G * Hk)
   int layout, causal;
   int n_qtiles, n_ktiles;   // tiles per shard
   int stat_L;               // per-shard rows of the statistics arrays: n_qtiles * 128

@@ -270,6 +270,21 @@ __device__ __forceinline__ void walk_q_tiles(const P& p, const KRange& k, int nq
   }
 }
 
+// walk_q_tiles over every query head that shares key / value head hk
+// (grouped-query attention: heads hk * G .. hk * G + G - 1; G = 1 is plain
+// multi-head attention): calls f(hq, r, qt) in head order, then ring order.
+template <int QT, class P, class F>
+__device__ __forceinline__ void walk_group_q_tiles(const P& p, const KRange& k, int nqt, int hk, F&& f) {
+  bool go = true;
+  for (int g = 0; g < p.G && go; ++g) {
+    const int hq = hk * p.G + g;
+    walk_q_tiles<QT>(p, k, nqt, [&](int r, int qt) {
+      go = f(hq, r, qt);
+      return go;
+    });
+  }
+}
+
 // Allowed query columns [c_lo, c_hi) of a key row (token gk) in query tile
 // qt (QT rows) of shard r (batched calls).
 template <int QT, class P>

@@ -88,6 +88,11 @@ def test_fwd_rejects_bad_arguments_before_launch(lib):
     assert _fwd(lib, _fake(shp, ra.RA_FP32), ok(), ok(), ok(), lse) == 1
     # shape mismatch
     assert _fwd(lib, ok(), _fake((1, 2, 128, 64)), ok(), ok(), lse) == 1
+    # grouped key / value heads: hk must divide h, and k and v agree
+    q3 = _fake((1, 3, 256, 64))
+    assert _fwd(lib, q3, ok(), ok(), _fake((1, 3, 256, 64)), _fake((1, 3, 256), ra.RA_FP32)) == 1
+    assert _fwd(lib, ok(), _fake((1, 4, 256, 64)), _fake((1, 4, 256, 64)), ok(), lse) == 1
+    assert _fwd(lib, ok(), ok(), _fake((1, 1, 256, 64)), ok(), lse) == 1
     # unsupported head dim
     assert _fwd(lib, _fake((1, 2, 256, 96)), _fake((1, 2, 256, 96)), _fake((1, 2, 256, 96)),
                 _fake((1, 2, 256, 96)), lse) == 2
