@@ -163,7 +163,8 @@ def _scale(scale, d):
 
 def ring_attn_fwd(q, k, v, layout="contiguous", n_shards=1, causal=False, softmax_scale=None, out=None, lse=None,
                   stream=None):
-    """Ring forward with the fp32 LSE merge fused.  q, k, v: (b, h, s, d) bf16 in layout order.
+    """Ring forward with the fp32 LSE merge fused.  q, k, v: (b, h, s, d) bf16 in layout order
+    (k and v may have hk heads, hk dividing h: query head i uses key / value head i // (h // hk)).
 
     Returns (out (b, h, s, d) bf16, lse (b, h, s) fp32), both in layout order."""
     lib = load()
@@ -223,7 +224,7 @@ def _ws_arg(workspace):
 
 def ring_attn_bwd(dout, q, k, v, out, lse, layout="contiguous", n_shards=1, causal=False, softmax_scale=None,
                   dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Gradients (dq, dk, dv), bf16, layout order."""
+    """Gradients (dq like q, dk and dv like k and v), bf16, layout order."""
     lib = load()
     b, h, s, d = q.shape
     dq = torch.empty_like(q) if dq is None else dq
@@ -300,7 +301,8 @@ def _cu_pair(cu_seqlens, device):
 def ring_attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen=None, n_shards=1, causal=True, softmax_scale=None,
                          out=None, lse=None, stream=None, layout="contiguous", workspace=None):
     """Packed sequences, one cu_seqlens.  q, k, v: (total, h, d) or (h, total, d) bf16 in
-    layout order ("contiguous" slices of the packed buffer, or "zigzag" per sequence).
+    layout order ("contiguous" slices of the packed buffer, or "zigzag" per sequence);
+    k and v may have fewer heads than q (grouped-query attention, as in ring_attn_fwd).
 
     workspace: None allocates what ring_attn_varlen_workspace_size asks for (for
     zigzag, the original-order copies the library computes in); pass a tensor to
