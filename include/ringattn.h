@@ -202,9 +202,10 @@ ra_status ring_attn_bwd_static_scratch(const ra_tensor* dout, const ra_tensor* q
  * bytes (its per-row statistics).  For RA_LAYOUT_ZIGZAG a workspace of at
  * least ring_attn_varlen_workspace_size(op, total, h, d, RA_LAYOUT_ZIGZAG, N)
  * bytes (256-byte aligned) makes the call run in original token order: it
- * copies its inputs out of the zigzag order into the workspace and runs the
- * contiguous-layout kernels there, which write every result row straight to
- * its row of the caller's zigzag-ordered outputs.  On one GPU the
+ * copies its tensor-core operands (q, k, v; in the backward dO, q, k, v) out
+ * of the zigzag order into the workspace and runs the contiguous-layout
+ * kernels there, which read out and lse and write every result row straight
+ * through the token map, in the caller's zigzag order.  On one GPU the
  * zigzag split is only a storage order, and with short sequences its 2N chunks
  * put several sequences into every 128-row tile, so most of the tiles' work
  * would be masked.  With a smaller (or no) workspace the zigzag kernels run on
@@ -273,9 +274,9 @@ ra_status ring_attn_varlen_unpermute(const ra_tensor* y, ra_tensor* x, const int
 /* Workspace bytes of a varlen call (see the varlen calls above): RA_OP_FWD: 0
  * for RA_LAYOUT_CONTIGUOUS, and for RA_LAYOUT_ZIGZAG the original-order copies
  * of q, k, v (3 * total * h * d bf16); RA_OP_BWD: the per-row statistics, plus
- * for RA_LAYOUT_ZIGZAG the copies of dO, q, k, v, out (5 tensors) and lse
- * (h * total fp32); zigzag also takes 2 * total int32 for the token map between
- * layout and original order and its inverse.
+ * for RA_LAYOUT_ZIGZAG the copies of dO, q, k, v (4 tensors; out and lse are
+ * read where they are); zigzag also takes 2 * total int32 for the token map
+ * between layout and original order and its inverse.
  * Each part 256-byte aligned.  0 on bad sizes (head_dim other than 64 or 128,
  * total not a multiple of n_shards, another layout). */
 size_t ring_attn_varlen_workspace_size(int32_t op, int64_t total, int64_t h, int64_t d, int32_t layout,

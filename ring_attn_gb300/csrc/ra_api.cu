@@ -354,7 +354,10 @@ ra_status bwd_common(const Bhsd& dout, const Bhsd& q, const Bhsd& k, const Bhsd&
   RA_TRY(make_tmap(dout, &tdo));
   {
     TimedLaunch tl(RA_KERNEL_BWD_PRE, st);
-    RA_TRY(cuda_status(launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, p.ctl, st)));
+    // with a row map (varlen in original order), out and lse stay in the
+    // caller's layout order and are read through it
+    RA_TRY(cuda_status(
+        launch_bwd_pre(vdo, vo, LseView{lse, lsb, lsh, lss}, nD, nlse2, stat_N, stat_L, p.ctl, row_map, st)));
   }
   if (q.d == 128 && q.h == k.h && __atomic_load_n(&g_dkdv_pair, __ATOMIC_RELAXED)) {
     CUtensorMap pq, pk, pv, pdo;  // 64-row boxes: the pair kernel loads 64 x 64 blocks
@@ -414,7 +417,6 @@ ra_status check_cu(const int32_t* cu_dev, const int32_t* cu_host, int32_t n_seqs
 // several), which write each output row straight to its row of the caller's
 // zigzag order through the inverse token map.
 size_t zz_tensor_bytes(long long total, long long h, long long d) { return round256((size_t)total * h * d * 2); }
-size_t zz_lse_bytes(long long total, long long h) { return round256((size_t)total * h * 4); }
 size_t zz_map_bytes(long long total) { return round256((size_t)total * 4); }
 // The outputs are written straight into the caller's layout-order rows (the
 // kernels take the inverse map), so only inputs are copied.
@@ -422,10 +424,10 @@ size_t zz_map_bytes(long long total) { return round256((size_t)total * 4); }
 size_t zz_fwd_bytes(long long total, long long h, long long d) {
   return 3 * zz_tensor_bytes(total, h, d) + 2 * zz_map_bytes(total);
 }
-// backward: the statistics, then dO, q, k, v, out, lse, the map and its inverse
+// backward: the statistics, then dO, q, k, v, the map and its inverse (out and
+// lse are only read by the statistics pass, through the map, where they are)
 size_t zz_bwd_bytes(long long total, long long h, long long d, int n_shards) {
-  return bwd_ws_bytes(1, h, total, n_shards) + 5 * zz_tensor_bytes(total, h, d) + zz_lse_bytes(total, h) +
-         2 * zz_map_bytes(total);
+  return bwd_ws_bytes(1, h, total, n_shards) + 4 * zz_tensor_bytes(total, h, d) + 2 * zz_map_bytes(total);
 }
 
 // A contiguous (h, total, d) bf16 view at p.
@@ -753,18 +755,18 @@ ra_status ring_attn_varlen_bwd(const ra_tensor* dout, const ra_tensor* q, const 
     const long long h = vq.h, d = vq.d;
     const long long hk = vk.h;  // k and v may have fewer heads than q
     const Bhsd do2 = zz_view(w, total, h, d), q2 = zz_view(w + T, total, h, d), k2 = zz_view(w + 2 * T, total, hk, d),
-               v2 = zz_view(w + 3 * T, total, hk, d), o2 = zz_view(w + 4 * T, total, h, d);
-    float* l2 = reinterpret_cast<float*>(w + 5 * T);
+               v2 = zz_view(w + 3 * T, total, hk, d);
     ZzCtx z{cu_seqlens_dev, n_seqs, n_shards, st, nullptr, nullptr};
-    RA_TRY(zz_map(z, w + 5 * T + zz_lse_bytes(total, h), total));
+    RA_TRY(zz_map(z, w + 4 * T, total));
     RA_TRY(zz_in(z, vdo, do2.data));
     RA_TRY(zz_in(z, vq, q2.data));
     RA_TRY(zz_in(z, vk, k2.data));
     RA_TRY(zz_in(z, vv, v2.data));
-    RA_TRY(zz_in(z, vo, o2.data));
-    RA_TRY(zz_permute(lse->data, lsh, lss, l2, total, 1, h, total, 0, 1, z.cu, z.n, z.N, z.map, st));
-    return bwd_common(do2, q2, k2, v2, o2, l2, 0, total, 1, RA_LAYOUT_CONTIGUOUS, n_shards, causal, softmax_scale,
-                      vdq, vdk, vdv, workspace, SB, cu_seqlens_dev, n_seqs, stream, -1, z.inv);
+    // out and lse stay in the caller's zigzag order: the statistics pass reads
+    // them through the inverse map
+    return bwd_common(do2, q2, k2, v2, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, RA_LAYOUT_CONTIGUOUS,
+                      n_shards, causal, softmax_scale, vdq, vdk, vdv, workspace, SB, cu_seqlens_dev, n_seqs, stream, -1,
+                      z.inv);
   }
   return bwd_common(vdo, vq, vk, vv, vo, static_cast<const float*>(lse->data), lsb, lsh, lss, layout, n_shards,
                     causal, softmax_scale, vdq, vdk, vdv, workspace, workspace_bytes, cu_seqlens_dev, n_seqs,

@@ -97,8 +97,10 @@ struct LseView {
   const float* data;
   long long sb, sh, ss;
 };
+// out_row: null, or out and lse rows by position (out and lse of position p
+// are row out_row[p] of their tensors; dout is read at p)
 cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
-                           int stat_L, const DevCtl& ctl, cudaStream_t st);
+                           int stat_L, const DevCtl& ctl, const int* out_row, cudaStream_t st);
 
 struct MergeArgs {
   float* out_acc;        // rows x d, row stride (elements)

@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeArgs a) {
 constexpr int kPreUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads, 4) bwd_pre_kernel(View4 dout, View4 out, LseView lse, float* nD,
-                                                               float* nlse2, int N, int stat_L, DevCtl ctl) {
+                                                               float* nlse2, int N, int stat_L, DevCtl ctl,
+                                                               const int* out_row) {
   const int tpr = dout.d / 8;  // threads per row; divides 32, so a row's threads share a warp
   const int rows_per_block = kThreads / tpr;
   const int rows_per_turn = kPreUnroll * rows_per_block;
@@ -220,10 +221,13 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_pre_kernel(View4 dout, View4 
     for (int u = 0; u < kPreUnroll; ++u) {
       const int i = i0 + u * rows_per_block + rloc;
       const long long p = (long long)r * L + i;  // layout position
-      const bool real = i < L && in_bounds(p < dout.s, ctl, 31);
+      bool real = i < L && in_bounds(p < dout.s, ctl, 31);
+      // out and lse of position p: row out_row[p] of the caller's layout order, or p
+      const long long po = real && out_row ? (long long)__ldg(out_row + p) : p;
+      real = real && in_bounds(po >= 0 && po < out.s, ctl, 32);
       x[u] = real ? __ldcs(reinterpret_cast<const uint4*>(dsrc + p * dout.ss) + part) : make_uint4(0, 0, 0, 0);
-      y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + p * out.ss) + part) : make_uint4(0, 0, 0, 0);
-      l[u] = real && part == 0 ? __ldcs(lsrc + p * lse.ss) : INFINITY;
+      y[u] = real ? __ldcs(reinterpret_cast<const uint4*>(osrc + po * out.ss) + part) : make_uint4(0, 0, 0, 0);
+      l[u] = real && part == 0 ? __ldcs(lsrc + po * lse.ss) : INFINITY;
     }
 #pragma unroll
     for (int u = 0; u < kPreUnroll; ++u) {
@@ -334,7 +338,7 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& lse, float* nD, float* nlse2, int N,
-                           int stat_L, const DevCtl& ctl, cudaStream_t st) {
+                           int stat_L, const DevCtl& ctl, const int* out_row, cudaStream_t st) {
   const int rows_per_turn = kPreUnroll * (kThreads / (dout.d / 8));
   if (stat_L % rows_per_turn != 0) return cudaErrorInvalidValue;  // a turn must not straddle a shard
   const long long turns = (long long)dout.b * dout.h * N * stat_L / rows_per_turn;
@@ -349,7 +353,7 @@ cudaError_t launch_bwd_pre(const View4& dout, const View4& out, const LseView& l
   long long blocks = (long long)num_sms() * per_sm[dev];  // one full wave
   if (blocks > turns) blocks = turns;
   if (blocks < 1) blocks = 1;
-  bwd_pre_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L, ctl);
+  bwd_pre_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(dout, out, lse, nD, nlse2, N, stat_L, ctl, out_row);
   return cudaGetLastError();
 }
 

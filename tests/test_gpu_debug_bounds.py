@@ -23,7 +23,7 @@ def test_parity_sweeps_pass_under_the_bounds_checks():
     env = dict(os.environ, RA_LIB_VARIANT="debug_bounds")
     cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
            "tests/test_gpu_attention.py", "tests/test_gpu_permute_merge.py", "tests/test_gpu_dkdv_pair.py",
-           "-k", "not full_size"]
+           "tests/test_gpu_gqa.py", "-k", "not full_size"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True,
                        timeout=1800)
     tail = "\n".join(r.stdout.splitlines()[-30:])
