@@ -102,14 +102,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test with a suspend-time hint: a thread whose phase is not complete
+// may stay suspended up to hint_ns nanoseconds (it resumes as soon as the
+// phase completes) instead of the system's default limit.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+template <uint32_t H>
+__device__ __forceinline__ bool mbar_try_wait_h(uint32_t bar, uint32_t parity) {
+  return H ? mbar_try_wait_hint(bar, parity, H) : mbar_try_wait(bar, parity);
+}
 
 // One thread waits.  Returns false when the CTA aborts (own timeout or another role's).
+// H: suspend-time hint of each test in nanoseconds (0: the system's default).
+template <uint32_t H = 0>
 static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
                                       int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_h<H>(bar, parity)) return true;
   unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_h<H>(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > c.wait_limit_ns) {
@@ -122,11 +142,12 @@ static __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, v
 }
 
 // A whole converged warp waits; the result is the same on every lane.
+template <uint32_t H = 0>
 static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, const DevCtl& c,
                                        int site) {
   unsigned long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
-    bool done = mbar_try_wait(bar, parity);
+    bool done = mbar_try_wait_h<H>(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     if ((it & 15u) == 15u) {
       int stop = 0;
