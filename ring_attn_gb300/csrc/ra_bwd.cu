@@ -427,9 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ======================================================================== dQ
-// Warps: 0 TMA (Q, dO once, then K into a 3-stage ring), 3 TMA (V into a
-// 2-stage ring), 1 MMA, 2 TMEM; warpgroups 1 and 2: one query row each, key
-// columns [0, 64) and [64, 128).  Q and dO are the same for every key tile, so
+// Warps: 0 TMA (Q, dO once, then each key tile's K into a 3-stage ring and V
+// into a 2-stage ring, both completing on the V stage's barrier, so the MMA
+// thread waits once per key tile), 1 MMA, 2 TMEM, 3 idle; warpgroups 1 and 2:
+// one query row each, key columns [0, 64) and [64, 128).  Q and dO are the
+// same for every key tile, so
 // the softmax threads copy them once into tensor memory (packed bf16) and the
 // S and dP MMAs take them from there: shared memory then feeds only the K and V
 // operands.  TMEM: S [0,128), dP [128,256), Q [256, 256+D/2), dO [256+D/2, 256+D),
@@ -456,7 +458,7 @@ struct DqLayout {
 
 enum DqBar {
   F_QDO_FULL = 0,
-  F_K_FULL = 1,    // 3
+  // 1..3: unused (K lands on the V stage's barrier)
   F_K_EMPTY = 4,   // 3
   F_V_FULL = 7,    // 2
   F_V_EMPTY = 9,   // 2
@@ -503,7 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(F_QDO_FULL), 1);
     for (int i = 0; i < KS; ++i) {
-      mbar_init(BAR(F_K_FULL + i), 1);
       mbar_init(BAR(F_K_EMPTY + i), 1);
     }
     for (int i = 0; i < VS; ++i) {
@@ -553,29 +554,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers
-    if (lane == 0 && n_tiles > 0) {
-      const bool is_k = warp == 0;
-      int issued[3] = {0, 0, 0};
-      const int nst = is_k ? KS : VS;
-      const int full0 = is_k ? F_K_FULL : F_V_FULL, empty0 = is_k ? F_K_EMPTY : F_V_EMPTY;
-      const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
-      const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+    if (warp == 0 && lane == 0 && n_tiles > 0) {
+      // K(j) and V(j) land on one barrier (the V stage's): the MMA thread
+      // waits once per key tile
+      int issued[2] = {0, 0};
       int j = 0;
       walk_kv_tiles(p, qr, nkt, 0, p.N, [&](int s, int kt) {
-        const int st = j % nst;
-        if (j >= nst && !wait_one(BAR(empty0 + st), (j / nst - 1) & 1, abort_flag, p.ctl, is_k ? 51 : 52))
-          return false;
-        mbar_expect_tx(BAR(full0 + st), LY::kTile);
+        const int sk = j % KS, sv = j % VS;
+        if (j >= KS && !wait_one(BAR(F_K_EMPTY + sk), (j / KS - 1) & 1, abort_flag, p.ctl, 51)) return false;
+        if (j >= VS && !wait_one(BAR(F_V_EMPTY + sv), (j / VS - 1) & 1, abort_flag, p.ctl, 52)) return false;
+        mbar_expect_tx(BAR(F_V_FULL + sv), 2 * LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl, 17))
-            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, hk,
-                        b);
-        ++issued[st];
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl,
+                        17)) {
+            tma_load_4d(sb + LY::kK + sk * LY::kTile + c * kBox, &tmK, BAR(F_V_FULL + sv), c * 64,
+                        s * p.L + kt * kTileN, hk, b);
+            tma_load_4d(sb + LY::kV + sv * LY::kTile + c * kBox, &tmV, BAR(F_V_FULL + sv), c * 64,
+                        s * p.L + kt * kTileN, hk, b);
+          }
+        ++issued[sv];
         ++j;
         return true;
       });
-      for (int st = 0; st < nst; ++st)
-        if (issued[st]) drain_one(BAR(full0 + st), (issued[st] - 1) & 1, p.ctl, 54);
+      for (int st = 0; st < VS; ++st)
+        if (issued[st]) drain_one(BAR(F_V_FULL + st), (issued[st] - 1) & 1, p.ctl, 54);
     }
     if (threadIdx.x == 0) drain_one(BAR(F_QDO_FULL), 0, p.ctl, 53);  // issued at entry
     __syncwarp();
@@ -595,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_s = [&](int j) -> bool {
         const int ks = j % KS;
-        if (!wait_one(BAR(F_K_FULL + ks), (j / KS) & 1, abort_flag, p.ctl, 56)) return false;
+        if (!wait_one(BAR(F_V_FULL + j % VS), (j / VS) & 1, abort_flag, p.ctl, 56)) return false;
         if (j > 0 && !wait_one(BAR(F_S_READ), (j - 1) & 1, abort_flag, p.ctl, 57)) return false;
         tc_fence_after();
         issue_t(LY::kTmemS, LY::kTmemQ, sb + LY::kK + ks * LY::kTile);
@@ -604,9 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // dP(j) overwrites dS(j-1), which the dQ MMA issued before it has read
       auto issue_dp = [&](int j) -> bool {
-        const int vs = j % VS;
-        if (!wait_one(BAR(F_V_FULL + vs), (j / VS) & 1, abort_flag, p.ctl, 58)) return false;
-        tc_fence_after();
+        const int vs = j % VS;  // V(j) landed with K(j), waited for before S(j)
         issue_t(LY::kTmemDP, LY::kTmemDO, sb + LY::kV + vs * LY::kTile);
         mma_commit(BAR(F_DP_FULL));
         if (j + VS < n_tiles) mma_commit(BAR(F_V_EMPTY + vs));
