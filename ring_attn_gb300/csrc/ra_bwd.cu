@@ -207,11 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdKV = idesc_bf16_f32(128, D, 0, 1);      // dV, dK: TMEM A, MN-major B
       // X^T = A B^T over D: A (K or V) and B (Q or dO tile) K-major in shared memory
       auto issue_t = [&](uint32_t dcol, uint32_t a, uint32_t bq) {
+        const uint64_t da = sdesc_sw128(a, 16, 1024), db = sdesc_sw128(bq, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + dcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024), kIdS,
-                      kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + dcol, sdesc_add(da, off), sdesc_add(db, off), kIdS, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = wait_one(BAR(E_KV_FULL), 0, abort_flag, p.ctl, 32) &&
@@ -246,17 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t qb = sb + LY::kQ + st * LY::kTile, ob = sb + LY::kDO + st * LY::kTile;
+        const uint64_t dqb = sdesc_sw128(sb + LY::kQ + st * LY::kTile, kBox, 1024);
+        const uint64_t dob = sdesc_sw128(sb + LY::kDO + st * LY::kTile, kBox, 1024);
         // dK += dS^T Q, then dV += P^T dO: A from the packed dP^T columns, B with 16 query rows per step
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)
-          mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk) + 32, sdesc_sw128(qb + kk * 2048, kBox, 1024),
-                      kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk) + 32, sdesc_add(dqb, kk * 2048), kIdKV,
+                      (i > 0 || kk > 0) ? 1u : 0u);
         if (i + 2 < n_tiles) mma_commit(BAR(E_Q_EMPTY + st));
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)
-          mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(ob + kk * 2048, kBox, 1024),
-                      kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_add(dob, kk * 2048), kIdKV,
+                      (i > 0 || kk > 0) ? 1u : 0u);
         if (i + 2 < n_tiles) mma_commit(BAR(E_DO_EMPTY + st));
         if (i + 1 == n_tiles) {
           mma_commit(BAR(E_KV_DONE));
@@ -589,10 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_one(BAR(F_QDO_TMEM), 0, abort_flag, p.ctl, 55);
       // X = A B^T over D with A (Q or dO) packed in TMEM, 16 head-dim columns = 8 TMEM columns per step
       auto issue_t = [&](uint32_t dcol, uint32_t acol, uint32_t bt) {
+        const uint64_t db = sdesc_sw128(bt, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ts(tmem + dcol, tmem + acol + 8 * kk, sdesc_sw128(bt + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ts(tmem + dcol, tmem + acol + 8 * kk, sdesc_add(db, off), kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_s = [&](int j) -> bool {
@@ -615,11 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_dq = [&](int j) -> bool {
         if (!wait_one(BAR(F_DS_FULL), j & 1, abort_flag, p.ctl, 59)) return false;
         tc_fence_after();
-        const uint32_t kb = sb + LY::kK + (j % KS) * LY::kTile;
+        const uint64_t dkb = sdesc_sw128(sb + LY::kK + (j % KS) * LY::kTile, kBox, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
           // A = dS (16 keys = 8 packed columns of the dP region), B = K with 16 key rows per step
-          mma_bf16_ts(tmem + LY::kTmemDQ, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(kb + kk * 2048, kBox, 1024),
+          mma_bf16_ts(tmem + LY::kTmemDQ, tmem + LY::kTmemDP + pcol(kk), sdesc_add(dkb, kk * 2048),
                       kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
         }
         if (j + KS < n_tiles) mma_commit(BAR(F_K_EMPTY + j % KS));

@@ -370,6 +370,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The descriptor of sdesc_sw128(saddr + bytes, ...) from that of saddr: the
+// start address field holds saddr / 16 in its low 14 bits, and every shared
+// memory address (< 256 KB) keeps the sum inside them, so the MMA loops step
+// a descriptor with one add instead of rebuilding it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a 128B-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
