@@ -375,6 +375,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 // memory address (< 256 KB) keeps the sum inside them, so the MMA loops step
 // a descriptor with one add instead of rebuilding it.
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+// The same descriptor as two 32-bit words, for loops short of registers: the
+// high word is a constant of the stride (SBO), the low word holds the address
+// and LBO and steps by bytes / 16.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_words(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` inside a 128B-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {

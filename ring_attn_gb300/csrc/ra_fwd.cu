@@ -229,13 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V: MN-major
       bool ok = wait_one<kWaitHint>(BAR(B_Q_FULL), 0, abort_flag, p.ctl, 2);
       auto issue_s = [&](int t, int j) {
-        const uint32_t kb = sb + LY::kK + (j % kKStages) * LY::kTile;
-        const uint32_t qb = sb + LY::kQ + t * LY::kTile;
+        // descriptors built once and stepped (low words only: this thread runs on few registers)
+        constexpr uint32_t kHi = sdesc_sw128_hi(1024);
+        const uint32_t lk = sdesc_sw128_lo(sb + LY::kK + (j % kKStages) * LY::kTile, 16);
+        const uint32_t lq = sdesc_sw128_lo(sb + LY::kQ + t * LY::kTile, 16);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + LY::kTmemS + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                      kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kBox + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + LY::kTmemS + t * 128, sdesc_words(lq + off, kHi), sdesc_words(lk + off, kHi), kIdS,
+                      kk > 0 ? 1u : 0u);
         }
         mma_commit(BAR(B_S_FULL + t));
       };
@@ -245,12 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             !wait_one<kWaitHint>(BAR(B_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.ctl, 4))
           return false;
         tc_fence_after();
-        const uint32_t vb = sb + LY::kV + (i % kVStages) * LY::kTile;
+        const uint32_t lv = sdesc_sw128_lo(sb + LY::kV + (i % kVStages) * LY::kTile, kBox);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
           // A = P: 16 keys = 8 packed columns of the S_t tile; B = V: 16 key rows = 2048 bytes
           mma_bf16_ts(tmem + LY::kTmemO + t * 128, tmem + LY::kTmemS + t * 128 + kk * 8,
-                      sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+                      sdesc_words(lv + kk * 128, sdesc_sw128_hi(1024)), kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
         if (t == kQTiles - 1 && i + kVStages < n_tiles) mma_commit(BAR(B_V_EMPTY + i % kVStages));
         return true;
