@@ -237,12 +237,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         constexpr uint32_t kIdKV = idesc_bf16_f32(256, D, 0, 1);      // dV, dK: TMEM A, MN-major B
         // X^T = A B^T over d: A (K or V, 128 rows per CTA) and B (64 query rows per CTA) K-major
         auto issue_t = [&](uint32_t dcol, uint32_t a, uint32_t bst) {
+          // descriptors built once and stepped by the K offset
+          const uint64_t da = sdesc_sw128(a, 16, 1024), db = sdesc_sw128(bst, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * kSub + (kk & 3) * 32;  // block X, then X2
-            mma_bf16_ss_pair(tmem + dcol, sdesc_sw128(a + aoff, 16, 1024), sdesc_sw128(bst + boff, 16, 1024), kIdS,
-                             kk > 0 ? 1u : 0u);
+            mma_bf16_ss_pair(tmem + dcol, sdesc_add(da, aoff), sdesc_add(db, boff), kIdS, kk > 0 ? 1u : 0u);
           }
         };
         bool ok = wait_one_pair(BAR(P_KV_FULL), 0, abort_flag, peer_abort, p.ctl, 86) &&
@@ -279,17 +280,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // dK += dS^T Q, then dV += P^T dO: A from the packed dP^T columns of
           // each CTA, B = blocks Y, Y2 (this CTA's 64 head dims), 16 query rows per step
-          const uint32_t qy = sb + LY::kQ + st * LY::kTile + LY::kY;
-          const uint32_t oy = sb + LY::kDO + st * LY::kTile + LY::kY;
+          const uint64_t dqy = sdesc_sw128(sb + LY::kQ + st * LY::kTile + LY::kY, kSub, 1024);
+          const uint64_t doy = sdesc_sw128(sb + LY::kDO + st * LY::kTile + LY::kY, kSub, 1024);
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
             mma_bf16_ts_pair(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk) + 32,
-                             sdesc_sw128(qy + kk * 2048, kSub, 1024), kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+                             sdesc_add(dqy, kk * 2048), kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
           if (i + 2 < n_tiles) mma_commit_pair(BAR(P_Q_EMPTY + st), kBoth);
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_bf16_ts_pair(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_sw128(oy + kk * 2048, kSub, 1024),
-                             kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts_pair(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_add(doy, kk * 2048), kIdKV,
+                             (i > 0 || kk > 0) ? 1u : 0u);
           if (i + 2 < n_tiles) mma_commit_pair(BAR(P_DO_EMPTY + st), kBoth);
           if (i + 1 == n_tiles) {
             mma_commit_pair(BAR(P_KV_DONE), kBoth);
