@@ -14,10 +14,11 @@
 //
 // Kernel structure: one CTA owns two 128-row query tiles (Q0, Q1: 256
 // consecutive rows of one shard) and 12 warps.
-//   warps 0, 3  TMA producers: warp 0 loads Q0 and Q1 once, then K tiles into a
-//               3-stage ring (freed when both S MMAs of a tile complete); warp 3
-//               loads V tiles into a 2-stage ring (freed when both PV MMAs
-//               complete), so K loads are never held back by the V ring.
+//   warp 0      TMA producer: Q0 and Q1 once, then per key tile K into a
+//               3-stage ring (freed when both S MMAs of a tile complete) and V
+//               into a 2-stage ring (freed when both PV MMAs complete), the two
+//               completing on the V stage's barrier, so the MMA thread waits
+//               once per key tile for both.  Warp 3 is idle.
 //   warp 1      MMA issuer (one thread).  Per key tile j it issues
 //                 PV0(j-1), S0(j), PV1(j-1), S1(j)
 //               (PV0(j-1) does not wait for K(j)),
@@ -81,7 +82,7 @@ struct FwdLayout {
 
 enum FwdBar {
   B_Q_FULL = 0,
-  B_K_FULL = 1,    // kKStages
+  B_K_FULL = 1,    // kKStages (unused: K lands on the V stage's barrier)
   B_K_EMPTY = 4,   // kKStages
   B_V_FULL = 7,    // kVStages
   B_V_EMPTY = 9,   // kVStages
@@ -136,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q_FULL), 1);
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(BAR(B_K_FULL + i), 1);
       mbar_init(BAR(B_K_EMPTY + i), 1);
     }
     for (int i = 0; i < kVStages; ++i) {
@@ -188,37 +188,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ control warpgroup
     regs_dec<kRegsLow>();
     if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------ TMA producers
-    // warp 0 loads Q and the K ring, warp 3 the V ring: K tiles run ahead of
-    // the V ring, which frees a stage only once both PV MMAs of a tile are done
-    if (lane == 0 && n_tiles > 0) {
-      const bool is_k = warp == 0;
-      int issued[kKStages] = {};
-      const int nst = is_k ? kKStages : kVStages;
-      const int full0 = is_k ? B_K_FULL : B_V_FULL, empty0 = is_k ? B_K_EMPTY : B_V_EMPTY;
-      const uint32_t ring = sb + (is_k ? LY::kK : LY::kV);
-      const void* tmap = is_k ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+    // ------------------------------------------------------------ TMA producer (warp 0)
+    if (warp == 0 && lane == 0 && n_tiles > 0) {
+      // K(j) and V(j) land on one barrier (the V stage's), so that the MMA
+      // thread waits once per key tile
+      int issued[kVStages] = {};
       int j = 0;
       walk_tiles(p, cta, nkt, [&](int s, int kt) {
-        const int st = j % nst;
-        // use u of a stage waits for the release of use u - 1
-        if (j >= nst &&
-            !wait_one<kWaitHint>(BAR(empty0 + st), (j / nst - 1) & 1, abort_flag, p.ctl, is_k ? 1 : 10))
+        const int sk = j % kKStages, sv = j % kVStages;
+        if (j >= kKStages &&
+            !wait_one<kWaitHint>(BAR(B_K_EMPTY + sk), (j / kKStages - 1) & 1, abort_flag, p.ctl, 1))
           return false;
-        mbar_expect_tx(BAR(full0 + st), LY::kTile);
-        // the key / value head of query head h (grouped-query attention), derived
-        // here rather than held across the walk: the producers run on few registers
+        if (j >= kVStages &&
+            !wait_one<kWaitHint>(BAR(B_V_EMPTY + sv), (j / kVStages - 1) & 1, abort_flag, p.ctl, 10))
+          return false;
+        mbar_expect_tx(BAR(B_V_FULL + sv), 2 * LY::kTile);
         const int hk = (int)(blockIdx.y % p.H) / p.G;
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl, 2))
-            tma_load_4d(ring + st * LY::kTile + c * kBox, tmap, BAR(full0 + st), c * 64, s * p.L + kt * kTileN, hk, b);
-        ++issued[st];
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl,
+                        2)) {
+            tma_load_4d(sb + LY::kK + sk * LY::kTile + c * kBox, &tmK, BAR(B_V_FULL + sv), c * 64,
+                        s * p.L + kt * kTileN, hk, b);
+            tma_load_4d(sb + LY::kV + sv * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + sv), c * 64,
+                        s * p.L + kt * kTileN, hk, b);
+          }
+        ++issued[sv];
         ++j;
         return true;
       });
-      // every issued copy lands before the CTA may exit
-      for (int st = 0; st < nst; ++st)
-        if (issued[st]) drain_one(BAR(full0 + st), (issued[st] - 1) & 1, p.ctl, 21);
+      for (int st = 0; st < kVStages; ++st)
+        if (issued[st]) drain_one(BAR(B_V_FULL + st), (issued[st] - 1) & 1, p.ctl, 21);
     }
     if (threadIdx.x == 0 && q_issued) drain_one(BAR(B_Q_FULL), 0, p.ctl, 20);
     __syncwarp();
@@ -243,9 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int i) -> bool {
         if (!wait_one<kWaitHint>(BAR(B_P_FULL + t), i & 1, abort_flag, p.ctl, 3)) return false;
-        if (t == 0 &&
-            !wait_one<kWaitHint>(BAR(B_V_FULL + i % kVStages), (i / kVStages) & 1, abort_flag, p.ctl, 4))
-          return false;
         tc_fence_after();
         const uint32_t lv = sdesc_sw128_lo(sb + LY::kV + (i % kVStages) * LY::kTile, kBox);
 #pragma unroll
@@ -268,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               return false;
             }
             if (t == 0) {
-              if (!wait_one<kWaitHint>(BAR(B_K_FULL + j % kKStages), (j / kKStages) & 1, abort_flag, p.ctl, 5)) {
+              if (!wait_one<kWaitHint>(BAR(B_V_FULL + j % kVStages), (j / kVStages) & 1, abort_flag, p.ctl, 5)) {
                 ok = false;
                 return false;
               }
