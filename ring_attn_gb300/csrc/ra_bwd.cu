@@ -37,15 +37,15 @@ constexpr int kThreads = 384;
 // Warps: 0 TMA (K, V once; Q with the query tile's -lse2 / -D, and dO, into two
 // 2-stage rings), 1 MMA, 2 TMEM; warpgroups 1 and 2: one key row each, query
 // columns [0, 64) and [64, 128).  TMEM: S^T [0,128), dP^T [128,256), dV
-// [256, 256+D), dK [256+D, 256+2D).  A thread reads its 64 S^T columns into
-// registers and releases them at once, so S^T of the next query tile can be
-// computed while this one is processed; it then writes P^T and dS^T as packed
-// bf16 over its own 64 dP^T columns (P^T in the first 32, dS^T in the last 32),
-// the A operands of dV += P^T dO and dK += dS^T Q.  Per query tile i the MMA
-// thread issues
-//   S^T(i+1) [once S^T(i) is read], dK(i), dV(i) [once P^T, dS^T are in TMEM],
+// [256, 256+D), dK [256+D, 256+2D).  A thread reads its 64 S^T columns,
+// writes P^T as packed bf16 over the first 32 of them (the A operand of
+// dV += P^T dO) and signals; once dP^T is ready it writes dS^T packed over the
+// first 32 of its own 64 dP^T columns (the A operand of dK += dS^T Q).  Per
+// query tile i the MMA thread issues
+//   dV(i) [once P^T(i) is in TMEM], S^T(i+1), dK(i) [once dS^T(i) is in TMEM],
 //   dP^T(i+1)
-// (dK first: it frees the Q stage the next-but-one S^T needs).
+// so the next tile's exponentials overlap dK(i) and dP^T(i+1), and its dS^T
+// overlaps dV(i+1) and S^T(i+2): each hand-off has two MMA groups of slack.
 template <int D>
 struct DkdvLayout {
   static constexpr int kTile = (D / 64) * kBox;
@@ -77,9 +77,9 @@ enum DkdvBar {
   E_DO_FULL = 5,    // 2
   E_DO_EMPTY = 7,   // 2
   E_S_FULL = 9,
-  E_S_READ = 10,    // S^T in registers: 8 elected arrivals
+  E_P_FULL = 10,    // P^T packed over the S^T columns: 8 elected arrivals
   E_DP_FULL = 11,
-  E_PS_FULL = 12,   // P^T and dS^T in TMEM: 8 elected arrivals
+  E_DS_FULL = 12,   // dS^T packed over the dP^T columns: 8 elected arrivals
   E_KV_DONE = 13,
   E_TEARDOWN = 14
 };
@@ -114,9 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(E_DO_EMPTY + i), 1);
     }
     mbar_init(BAR(E_S_FULL), 1);
-    mbar_init(BAR(E_S_READ), 8);
+    mbar_init(BAR(E_P_FULL), 8);
     mbar_init(BAR(E_DP_FULL), 1);
-    mbar_init(BAR(E_PS_FULL), 8);
+    mbar_init(BAR(E_DS_FULL), 8);
     mbar_init(BAR(E_KV_DONE), 1);
     mbar_init(BAR(E_TEARDOWN), 1);
     *abort_flag = 0;
@@ -230,10 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int st = i & 1, st1 = (i + 1) & 1;
         const uint32_t par1 = ((i + 1) >> 1) & 1;
+        // dV += P^T dO once P^T(i) is packed over the S^T columns
+        if (!wait_one(BAR(E_P_FULL), i & 1, abort_flag, p.ctl, 45)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t dob = sdesc_sw128(sb + LY::kDO + st * LY::kTile, kBox, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kTileM / 16; ++kk)
+          mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemS + pcol(kk), sdesc_add(dob, kk * 2048), kIdKV,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 2 < n_tiles) mma_commit(BAR(E_DO_EMPTY + st));
         if (i + 1 < n_tiles) {
-          // S^T(i+1) into the S^T columns once every thread holds S^T(i) in registers
-          if (!wait_one(BAR(E_Q_FULL + st1), par1, abort_flag, p.ctl, 33) ||
-              !wait_one(BAR(E_S_READ), i & 1, abort_flag, p.ctl, 45)) {
+          // S^T(i+1) overwrites the P^T(i) the dV MMAs above read first
+          if (!wait_one(BAR(E_Q_FULL + st1), par1, abort_flag, p.ctl, 33)) {
             ok = false;
             break;
           }
@@ -241,28 +252,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_t(LY::kTmemS, sb + LY::kK, sb + LY::kQ + st1 * LY::kTile);
           mma_commit(BAR(E_S_FULL));
         }
-        if (!wait_one(BAR(E_PS_FULL), i & 1, abort_flag, p.ctl, 35)) {
+        // dK += dS^T Q once dS^T(i) is packed over the dP^T columns
+        if (!wait_one(BAR(E_DS_FULL), i & 1, abort_flag, p.ctl, 35)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t dqb = sdesc_sw128(sb + LY::kQ + st * LY::kTile, kBox, 1024);
-        const uint64_t dob = sdesc_sw128(sb + LY::kDO + st * LY::kTile, kBox, 1024);
-        // dK += dS^T Q, then dV += P^T dO: A from the packed dP^T columns, B with 16 query rows per step
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk)
-          mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk) + 32, sdesc_add(dqb, kk * 2048), kIdKV,
+          mma_bf16_ts(tmem + LY::kTmemDK, tmem + LY::kTmemDP + pcol(kk), sdesc_add(dqb, kk * 2048), kIdKV,
                       (i > 0 || kk > 0) ? 1u : 0u);
         if (i + 2 < n_tiles) mma_commit(BAR(E_Q_EMPTY + st));
-#pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk)
-          mma_bf16_ts(tmem + LY::kTmemDV, tmem + LY::kTmemDP + pcol(kk), sdesc_add(dob, kk * 2048), kIdKV,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-        if (i + 2 < n_tiles) mma_commit(BAR(E_DO_EMPTY + st));
         if (i + 1 == n_tiles) {
           mma_commit(BAR(E_KV_DONE));
         } else {
-          // dP^T(i+1) overwrites the packed operands the dK / dV MMAs above read first
+          // dP^T(i+1) overwrites the dS^T(i) the dK MMAs above read first
           if (!wait_one(BAR(E_DO_FULL + st1), par1, abort_flag, p.ctl, 34)) {
             ok = false;
             break;
@@ -319,10 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t v[64];
       tmem_ld64(tl + LY::kTmemS + 64 * half, v);
-      // S^T is in registers: the MMA thread may compute the next tile's S^T over it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(E_S_READ));
       // P^T = exp2(s * scale - lse2), s * scale - lse2 two lanes per instruction
       const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
 #pragma unroll
@@ -344,30 +345,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) v[c] = ((mw >> c) & 1ull) ? v[c] : 0u;
       }
+      // P^T packed over the first 32 of the thread's 64 S^T columns (column m:
+      // queries 2m, 2m + 1), the A operand of dV += P^T dO; the MMA thread then
+      // computes the next tile's S^T over it
+      {
+        const uint32_t ts = tl + LY::kTmemS + 64 * half;
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pp[c] = pack_bf16x2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+        tmem_st16(ts, *reinterpret_cast<uint32_t(*)[16]>(pp));
+        tmem_st16(ts + 16, *reinterpret_cast<uint32_t(*)[16]>(pp + 16));
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(E_P_FULL));
       if (!wait_warp(BAR(E_DP_FULL), i & 1, abort_flag, p.ctl, 37)) {
         ok = false;
         return false;
       }
       tc_fence_after();
-      // dS^T = P^T * (dP^T - D), 32 dP^T columns at a time.  The thread's 64 dP^T
-      // columns then hold P^T packed in [0, 32) (column m: queries 2m, 2m + 1) and
-      // dS^T packed in [32, 64); a packed half is stored once the columns under it are read.
+      // dS^T = P^T * (dP^T - D), 32 dP^T columns at a time, packed over the first
+      // 32 of the thread's 64 dP^T columns (a packed half is stored once the
+      // columns under it are read): the A operand of dK += dS^T Q
       const uint32_t tdp = tl + LY::kTmemDP + 64 * half;
-      uint32_t ps[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t d[32];
         tmem_ld32(tdp + 32 * hh, d);
         tmem_ld_wait(d);
-        uint32_t pp[16];
+        uint32_t ps[16];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 dd = ds4[8 * hh + c4];
           const int c = 32 * hh + 4 * c4;
           const float p0 = __uint_as_float(v[c]), p1 = __uint_as_float(v[c + 1]);
           const float p2 = __uint_as_float(v[c + 2]), p3 = __uint_as_float(v[c + 3]);
-          pp[2 * c4] = pack_bf16x2(p0, p1);
-          pp[2 * c4 + 1] = pack_bf16x2(p2, p3);
           // dS^T = P^T * (dP^T + (-D)), two lanes per instruction
           float s0, s1, s2, s3;
           f32x2_split(mul_f32x2(f32x2(p0, p1), add_f32x2(f32x2(__uint_as_float(d[4 * c4]), __uint_as_float(d[4 * c4 + 1])),
@@ -377,17 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                 __uint_as_float(d[4 * c4 + 3])),
                                                          f32x2(dd.z, dd.w))),
                       s2, s3);
-          ps[16 * hh + 2 * c4] = pack_bf16x2(s0, s1);
-          ps[16 * hh + 2 * c4 + 1] = pack_bf16x2(s2, s3);
+          ps[2 * c4] = pack_bf16x2(s0, s1);
+          ps[2 * c4 + 1] = pack_bf16x2(s2, s3);
         }
-        tmem_st16(tdp + 16 * hh, pp);
+        tmem_st16(tdp + 16 * hh, ps);
       }
-      tmem_st16(tdp + 32, *reinterpret_cast<uint32_t(*)[16]>(ps));
-      tmem_st16(tdp + 48, *reinterpret_cast<uint32_t(*)[16]>(ps + 16));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(E_PS_FULL));
+      if (lane == 0) mbar_arrive(BAR(E_DS_FULL));
       ++i;
       return true;
     };
