@@ -35,9 +35,10 @@ constexpr int kThreads = 384;
 
 // ======================================================================== dK / dV
 // Warps: 0 TMA (K, V once; Q with the query tile's -lse2 / -D, and dO, into two
-// 2-stage rings), 1 MMA, 2 TMEM; warpgroups 1 and 2: one key row each, query
-// columns [0, 64) and [64, 128).  TMEM: S^T [0,128), dP^T [128,256), dV
-// [256, 256+D), dK [256+D, 256+2D).  A thread reads its 64 S^T columns,
+// 2-stage rings filled onto the Q stage's barrier), 1 MMA, 2 TMEM; warpgroups
+// 1 and 2: one key row each, query columns [0, 64) and [64, 128).  TMEM: S^T
+// [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).  A thread
+// reads its 64 S^T columns,
 // writes P^T as packed bf16 over the first 32 of them (the A operand of
 // dV += P^T dO) and signals; once dP^T is ready it writes dS^T packed over the
 // first 32 of its own 64 dP^T columns (the A operand of dK += dS^T Q).  Per
@@ -72,9 +73,9 @@ static_assert(128 * kDkdvRegsLow + 256 * kDkdvRegsHigh <= kThreads * kDkdvLaunch
 
 enum DkdvBar {
   E_KV_FULL = 0,
-  E_Q_FULL = 1,     // 2: Q, -lse2 and -D of a query tile
+  E_Q_FULL = 1,     // 2: Q, dO, -lse2 and -D of a query tile
   E_Q_EMPTY = 3,    // 2
-  E_DO_FULL = 5,    // 2
+  // 5..6: unused (dO lands on the Q stage's barrier)
   E_DO_EMPTY = 7,   // 2
   E_S_FULL = 9,
   E_P_FULL = 10,    // P^T packed over the S^T columns: 8 elected arrivals
@@ -110,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(E_Q_FULL + i), 1);
       mbar_init(BAR(E_Q_EMPTY + i), 1);
-      mbar_init(BAR(E_DO_FULL + i), 1);
       mbar_init(BAR(E_DO_EMPTY + i), 1);
     }
     mbar_init(BAR(E_S_FULL), 1);
@@ -164,25 +164,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((i >> 1) - 1) & 1;
         const int qrow = r * p.L + qt * kTileM - p.q_base;
         const long long stat_bh = ((long long)b * p.H + h) * p.stat_N * p.stat_L;  // (b, h, first shard)
-        if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) return false;
+        if (i >= 2 && (!wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31) ||
+                       !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)))
+          return false;
         // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
         const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
-        mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
+        mbar_expect_tx(BAR(E_Q_FULL + st), 2 * LY::kTile + 2 * 512);
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 11))
+          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 11)) {
             tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
+            tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
+          }
         if (in_bounds(stat_rows_ok(p, e0), p.ctl, 12)) {
           bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(E_Q_FULL + st));
           bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(E_Q_FULL + st));
         }
-        if (i >= 2 && !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)) {
-          drain_one(BAR(E_Q_FULL + st), (i >> 1) & 1, p.ctl, 43);
-          return false;
-        }
-        mbar_expect_tx(BAR(E_DO_FULL + st), LY::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 13))
-            tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_DO_FULL + st), c * 64, qrow, h, b);
         ++issued[st];
         ++i;
         return true;
@@ -193,10 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         walk_group_q_tiles<kTileM>(p, k, p.n_qtiles, hk, load);
       for (int st = 0; st < 2; ++st)
-        if (issued[st]) {
-          drain_one(BAR(E_Q_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
-          drain_one(BAR(E_DO_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
-        }
+        if (issued[st]) drain_one(BAR(E_Q_FULL + st), (issued[st] - 1) & 1, p.ctl, 41);
     }
     if (lane == 0) drain_one(BAR(E_KV_FULL), 0, p.ctl, 40);  // issued at entry
     __syncwarp();
@@ -220,12 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_t(LY::kTmemS, sb + LY::kK, sb + LY::kQ);
         mma_commit(BAR(E_S_FULL));
-        ok = wait_one(BAR(E_DO_FULL), 0, abort_flag, p.ctl, 34);
-        if (ok) {
-          tc_fence_after();
-          issue_t(LY::kTmemDP, sb + LY::kV, sb + LY::kDO);
-          mma_commit(BAR(E_DP_FULL));
-        }
+        issue_t(LY::kTmemDP, sb + LY::kV, sb + LY::kDO);
+        mma_commit(BAR(E_DP_FULL));
       }
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int st = i & 1, st1 = (i + 1) & 1;
@@ -267,12 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i + 1 == n_tiles) {
           mma_commit(BAR(E_KV_DONE));
         } else {
-          // dP^T(i+1) overwrites the dS^T(i) the dK MMAs above read first
-          if (!wait_one(BAR(E_DO_FULL + st1), par1, abort_flag, p.ctl, 34)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // dP^T(i+1) overwrites the dS^T(i) the dK MMAs above read first (dO(i+1)
+          // landed with Q(i+1), waited for before S^T(i+1))
           issue_t(LY::kTmemDP, sb + LY::kV, sb + LY::kDO + st1 * LY::kTile);
           mma_commit(BAR(E_DP_FULL));
         }
