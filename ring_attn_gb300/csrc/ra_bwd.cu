@@ -164,17 +164,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((i >> 1) - 1) & 1;
         const int qrow = r * p.L + qt * kTileM - p.q_base;
         const long long stat_bh = ((long long)b * p.H + h) * p.stat_N * p.stat_L;  // (b, h, first shard)
-        if (i >= 2 && (!wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31) ||
-                       !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)))
+        // dV frees the dO stage two MMA groups before dK frees the Q stage: dO
+        // goes first, onto the same barrier (its bytes added without an arrival)
+        if (i >= 2 && !wait_one(BAR(E_DO_EMPTY + st), par, abort_flag, p.ctl, 39)) return false;
+        const bool rows_ok = in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, 0, qrow, h, b), p.ctl, 11);
+        mbar_add_tx(BAR(E_Q_FULL + st), LY::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          if (rows_ok)
+            tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
+        if (i >= 2 && !wait_one(BAR(E_Q_EMPTY + st), par, abort_flag, p.ctl, 31)) {
+          // the phase then completes once dO has landed, and the drain below waits for it
+          mbar_arrive(BAR(E_Q_FULL + st));
+          ++issued[st];
           return false;
+        }
         // -lse2 / -D of the tile's 128 query rows: 512-byte aligned in the padded layout
         const long long e0 = stat_bh + (long long)(r - p.stat_r0) * p.stat_L + qt * kTileM;
-        mbar_expect_tx(BAR(E_Q_FULL + st), 2 * LY::kTile + 2 * 512);
+        mbar_expect_tx(BAR(E_Q_FULL + st), LY::kTile + 2 * 512);
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 11)) {
+          if (rows_ok)
             tma_load_4d(sb + LY::kQ + st * LY::kTile + c * kBox, &tmQ, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
-            tma_load_4d(sb + LY::kDO + st * LY::kTile + c * kBox, &tmDO, BAR(E_Q_FULL + st), c * 64, qrow, h, b);
-          }
         if (in_bounds(stat_rows_ok(p, e0), p.ctl, 12)) {
           bulk_load(sb + LY::kStats + (st * 2 + 0) * 512, p.nlse2 + e0, 512, BAR(E_Q_FULL + st));
           bulk_load(sb + LY::kStats + (st * 2 + 1) * 512, p.nD + e0, 512, BAR(E_Q_FULL + st));
