@@ -18,7 +18,8 @@
 //               3-stage ring (freed when both S MMAs of a tile complete) and V
 //               into a 2-stage ring (freed when both PV MMAs complete), the two
 //               completing on the V stage's barrier, so the MMA thread waits
-//               once per key tile for both.  Warp 3 is idle.
+//               once per key tile for both (K, whose stage frees first, is
+//               issued first).  Warp 3 is idle.
 //   warp 1      MMA issuer (one thread).  Per key tile j it issues
 //                 PV0(j-1), S0(j), PV1(j-1), S1(j)
 //               (PV0(j-1) does not wait for K(j)),
@@ -196,22 +197,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       walk_tiles(p, cta, nkt, [&](int s, int kt) {
         const int sk = j % kKStages, sv = j % kVStages;
+        // K's stage frees about two key tiles before V's: K goes first, its
+        // bytes added to the V stage's phase without an arrival, once that
+        // phase is the one of tile j (the phase of tile j - 2 has completed)
         if (j >= kKStages &&
             !wait_one<kWaitHint>(BAR(B_K_EMPTY + sk), (j / kKStages - 1) & 1, abort_flag, p.ctl, 1))
           return false;
         if (j >= kVStages &&
-            !wait_one<kWaitHint>(BAR(B_V_EMPTY + sv), (j / kVStages - 1) & 1, abort_flag, p.ctl, 10))
+            !wait_one<kWaitHint>(BAR(B_V_FULL + sv), (j / kVStages - 1) & 1, abort_flag, p.ctl, 6))
           return false;
-        mbar_expect_tx(BAR(B_V_FULL + sv), 2 * LY::kTile);
         const int hk = (int)(blockIdx.y % p.H) / p.G;
+        const int krow = s * p.L + kt * kTileN;
+        const bool rows_ok = in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, 0, krow, hk, b), p.ctl, 2);
+        mbar_add_tx(BAR(B_V_FULL + sv), LY::kTile);
         for (int c = 0; c < D / 64; ++c)
-          if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, s * p.L + kt * kTileN, hk, b), p.ctl,
-                        2)) {
-            tma_load_4d(sb + LY::kK + sk * LY::kTile + c * kBox, &tmK, BAR(B_V_FULL + sv), c * 64,
-                        s * p.L + kt * kTileN, hk, b);
-            tma_load_4d(sb + LY::kV + sv * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + sv), c * 64,
-                        s * p.L + kt * kTileN, hk, b);
-          }
+          if (rows_ok) tma_load_4d(sb + LY::kK + sk * LY::kTile + c * kBox, &tmK, BAR(B_V_FULL + sv), c * 64, krow, hk, b);
+        if (j >= kVStages &&
+            !wait_one<kWaitHint>(BAR(B_V_EMPTY + sv), (j / kVStages - 1) & 1, abort_flag, p.ctl, 10)) {
+          // the phase then completes once K has landed, and the drain below waits for it
+          mbar_arrive(BAR(B_V_FULL + sv));
+          ++issued[sv];
+          return false;
+        }
+        mbar_expect_tx(BAR(B_V_FULL + sv), LY::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          if (rows_ok) tma_load_4d(sb + LY::kV + sv * LY::kTile + c * kBox, &tmV, BAR(B_V_FULL + sv), c * 64, krow, hk, b);
         ++issued[sv];
         ++j;
         return true;
