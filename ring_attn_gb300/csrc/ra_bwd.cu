@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int krow = ks * p.L + kj0;
     mbar_expect_tx(BAR(E_KV_FULL), 2 * LY::kTile);
     for (int c = 0; c < D / 64; ++c)
-      if (in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, krow, hk, b), p.ctl, 10)) {
+      if (!(p.ctl.debug_flags & DBG_SKIP_KV_LOAD) &&
+          in_bounds(tma_coords_ok(TmaExtent{D, p.S, p.Hk, p.B}, c * 64, krow, hk, b), p.ctl, 10)) {
         tma_load_4d(sb + LY::kK + c * kBox, &tmK, BAR(E_KV_FULL), c * 64, krow, hk, b);
         tma_load_4d(sb + LY::kV + c * kBox, &tmV, BAR(E_KV_FULL), c * 64, krow, hk, b);
       }

@@ -389,6 +389,32 @@ def test_bounded_wait_reports_timeout_and_context_survives(ra):
     assert_lse_close("lse", lse.cpu(), ref_l)
 
 
+def test_bounded_wait_backward_reports_timeout_and_context_survives(ra):
+    """The dK/dV kernel is told to skip its K / V load, so its MMA and
+    elementwise warps' bounded waits run out: the backward records
+    RA_ERR_TIMEOUT and returns.  The same context then computes a correct
+    backward."""
+    x = make_qkv(1, 1, 512, 64, 5, with_do=True)
+    g = {k: v.cuda() for k, v in x.items()}
+    out, lse = ra.ring_attn_fwd(g["q"], g["k"], g["v"], "contiguous", 2, True, 0.125)
+    check_no_device_error(ra)
+    try:
+        ra.ring_attn_set_knob(ra.RA_KNOB_WAIT_LIMIT_NS, 2_000_000)
+        ra.ring_attn_set_knob(ra.RA_KNOB_DEBUG_FLAGS, 2)
+        ra.ring_attn_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, "contiguous", 2, True, 0.125)
+        st, info = ra.ring_attn_check_device_error()
+    finally:
+        ra.ring_attn_set_knob(ra.RA_KNOB_DEBUG_FLAGS, 0)
+        ra.ring_attn_set_knob(ra.RA_KNOB_WAIT_LIMIT_NS, int(os.environ.get("RA_TEST_WAIT_LIMIT_NS", 4_000_000_000)))
+    assert st == 6, (st, info)
+    assert ra.ring_attn_check_device_error() == (0, 0)
+    dq, dk, dv = ra.ring_attn_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, "contiguous", 2, True, 0.125)
+    check_no_device_error(ra)
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], 0.125, True)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert_close(name, got.cpu(), want)
+
+
 def test_outputs_are_finite_and_deterministic_shape_errors(ra):
     x = make_qkv(1, 2, 512, 128, 4, with_do=False)
     g = {k: v.cuda() for k, v in x.items()}
