@@ -298,8 +298,8 @@ ra_status ring_attn_check_device_error(void* stream, int32_t* info);
 /* Knobs (process-wide).  RA_KNOB_WAIT_LIMIT_NS: the bounded-wait limit in ns
  * (default 4e9).  RA_KNOB_DEBUG_FLAGS: bit 0 makes the forward's TMA producer
  * skip the Q tile load, bit 1 the one-CTA dK / dV kernel skip its K / V load,
- * so that every consumer's bounded wait runs out: tests of the timeout path
- * that hang nothing.  RA_KNOB_DKDV_PAIR: 1 runs the
+ * bit 2 the dQ kernel skip its Q / dO load, so that every consumer's bounded
+ * wait runs out: tests of the timeout path that hang nothing.  RA_KNOB_DKDV_PAIR: 1 runs the
  * backward's dK / dV pass at head_dim 128 on CTA pairs (two SMs share each
  * M = 256 tensor-core MMA, halving each SM's operand reads from shared memory);
  * 0 (default) runs the one-CTA kernel, which head_dim 64 always uses.  Both

@@ -967,7 +967,7 @@ ra_status ring_attn_set_knob(int32_t knob, int64_t value) {
     return RA_OK;
   }
   if (knob == RA_KNOB_DEBUG_FLAGS) {
-    if (value < 0 || value > 3) return RA_ERR_INVALID_ARG;  // bits 0 and 1
+    if (value < 0 || value > 7) return RA_ERR_INVALID_ARG;  // bits 0, 1 and 2
     g_debug_flags = (int)value;
     return RA_OK;
   }

@@ -536,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qrow = r * p.L + i0 - p.q_base;
     mbar_expect_tx(BAR(F_QDO_FULL), 2 * LY::kTile);
     for (int c = 0; c < D / 64; ++c)
-      if (in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 16)) {
+      if (!(p.ctl.debug_flags & DBG_SKIP_QDO_LOAD) &&
+          in_bounds(tma_coords_ok(TmaExtent{D, p.q_rows, p.H, p.B}, c * 64, qrow, h, b), p.ctl, 16)) {
         tma_load_4d(sb + LY::kQ + c * kBox, &tmQ, BAR(F_QDO_FULL), c * 64, qrow, h, b);
         tma_load_4d(sb + LY::kDO + c * kBox, &tmDO, BAR(F_QDO_FULL), c * 64, qrow, h, b);
       }

@@ -21,10 +21,10 @@ struct DevCtl {
   int* err_word;          // first error code wins (atomicCAS from 0)
   int* err_info;          // site | (block << 8) of the first failure
   unsigned long long wait_limit_ns;
-  int debug_flags;        // bounded-wait tests: bit 0 forward skips its Q load, bit 1 dK/dV its K / V load
+  int debug_flags;        // bounded-wait tests: the forward (bit 0), dK/dV (bit 1) or dQ (bit 2) kernel skips its entry load
 };
 
-enum : int { DBG_SKIP_Q_LOAD = 1, DBG_SKIP_KV_LOAD = 2 };
+enum : int { DBG_SKIP_Q_LOAD = 1, DBG_SKIP_KV_LOAD = 2, DBG_SKIP_QDO_LOAD = 4 };
 
 __device__ __forceinline__ void record_error(const DevCtl& c, int code, int site) {
   if (atomicCAS(c.err_word, 0, code) == 0) {

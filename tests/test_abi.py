@@ -224,9 +224,9 @@ def test_permute_refuses_overlapping_buffers(lib):
 
 def test_knobs(lib):
     assert lib.ring_attn_set_knob(0, 10) == 1
-    assert lib.ring_attn_set_knob(1, 5) == 1
-    assert lib.ring_attn_set_knob(1, 4) == 1
-    assert lib.ring_attn_set_knob(1, 3) == 0
+    assert lib.ring_attn_set_knob(1, 8) == 1
+    assert lib.ring_attn_set_knob(1, -1) == 1
+    assert lib.ring_attn_set_knob(1, 7) == 0
     assert lib.ring_attn_set_knob(1, 2) == 0
     assert lib.ring_attn_set_knob(7, 0) == 1
     assert lib.ring_attn_set_knob(2, 5) == 1

@@ -389,18 +389,19 @@ def test_bounded_wait_reports_timeout_and_context_survives(ra):
     assert_lse_close("lse", lse.cpu(), ref_l)
 
 
-def test_bounded_wait_backward_reports_timeout_and_context_survives(ra):
-    """The dK/dV kernel is told to skip its K / V load, so its MMA and
-    elementwise warps' bounded waits run out: the backward records
-    RA_ERR_TIMEOUT and returns.  The same context then computes a correct
-    backward."""
+@pytest.mark.parametrize("flag", [2, 4], ids=["dkdv", "dq"])
+def test_bounded_wait_backward_reports_timeout_and_context_survives(ra, flag):
+    """The dK/dV kernel is told to skip its K / V load (flag 2), or the dQ
+    kernel its Q / dO load (flag 4), so that kernel's bounded waits run out:
+    the backward records RA_ERR_TIMEOUT and returns.  The same context then
+    computes a correct backward."""
     x = make_qkv(1, 1, 512, 64, 5, with_do=True)
     g = {k: v.cuda() for k, v in x.items()}
     out, lse = ra.ring_attn_fwd(g["q"], g["k"], g["v"], "contiguous", 2, True, 0.125)
     check_no_device_error(ra)
     try:
         ra.ring_attn_set_knob(ra.RA_KNOB_WAIT_LIMIT_NS, 2_000_000)
-        ra.ring_attn_set_knob(ra.RA_KNOB_DEBUG_FLAGS, 2)
+        ra.ring_attn_set_knob(ra.RA_KNOB_DEBUG_FLAGS, flag)
         ra.ring_attn_bwd(g["do"], g["q"], g["k"], g["v"], out, lse, "contiguous", 2, True, 0.125)
         st, info = ra.ring_attn_check_device_error()
     finally:
